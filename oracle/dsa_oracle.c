@@ -107,7 +107,8 @@ int oracle_index_score(int batch, int bs, int num_blocks, int max_blocks,
   if (batch <= 0 || bs <= 0 || Nq < 0 || H <= 0 || D <= 0 || ld <= 0)
     return OR_ERR_ARG;
   double* q = (double*)malloc(sizeof(double) * (size_t)H * D);
-  if (!q) return OR_ERR_ARG;
+  double* k = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!q || !k) { free(q); free(k); return OR_ERR_ARG; }
   int rc = OR_OK;
   for (int r = 0; r < Nq; ++r) {
     int b = q_seq[r];
@@ -123,17 +124,18 @@ int oracle_index_score(int batch, int bs, int num_blocks, int max_blocks,
       if (p > last) { *out = -INFINITY; continue; }
       int64_t row = or_phys_row(block_table, max_blocks, bs, num_blocks, b, p);
       if (row < 0) { *out = -INFINITY; rc = OR_ERR_LAYOUT; continue; }
+      for (int d = 0; d < D; ++d) k[d] = or_load(kidx_pool, dtype, row * D + d);
       double s = 0.0;
       for (int h = 0; h < H; ++h) {
         double dot = 0.0;
-        for (int d = 0; d < D; ++d)
-          dot += q[h * D + d] * or_load(kidx_pool, dtype, row * D + d);
+        for (int d = 0; d < D; ++d) dot += q[h * D + d] * k[d];
         if (dot > 0.0) s += (double)w[(int64_t)r * H + h] * dot;
       }
       *out = (float)s;
     }
   }
   free(q);
+  free(k);
   return rc;
 }
 
@@ -218,10 +220,12 @@ int oracle_sparse_attn(int batch, int bs, int num_blocks, int max_blocks,
       K <= 0)
     return OR_ERR_ARG;
   int rc = OR_OK;
-  int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)K);
+  /* the selected rows, decoded once: kk [K][Dqk], vv [K][Dv] */
+  double* kk = (double*)malloc(sizeof(double) * (size_t)K * Dqk);
+  double* vv = (double*)malloc(sizeof(double) * (size_t)K * Dv);
   double* z = (double*)malloc(sizeof(double) * (size_t)K);
   double* qh = (double*)malloc(sizeof(double) * (size_t)Dqk);
-  if (!rows || !z || !qh) { free(rows); free(z); free(qh); return OR_ERR_ARG; }
+  if (!kk || !vv || !z || !qh) { free(kk); free(vv); free(z); free(qh); return OR_ERR_ARG; }
   for (int r = 0; r < Nq; ++r) {
     int b = q_seq[r];
     if (b < 0 || b >= batch) { rc = OR_ERR_ARG; break; }
@@ -232,7 +236,9 @@ int oracle_sparse_attn(int batch, int bs, int num_blocks, int max_blocks,
       if (p >= seq_lens[b]) { rc = OR_ERR_LAYOUT; continue; }
       int64_t row = or_phys_row(block_table, max_blocks, bs, num_blocks, b, p);
       if (row < 0) { rc = OR_ERR_LAYOUT; continue; }
-      rows[n++] = row;
+      for (int d = 0; d < Dqk; ++d) kk[(int64_t)n * Dqk + d] = or_dec_bf16(k_pool[row * k_row_stride + d]);
+      for (int d = 0; d < Dv; ++d) vv[(int64_t)n * Dv + d] = or_dec_bf16(v_pool[row * v_row_stride + d]);
+      ++n;
     }
     for (int h = 0; h < Hq; ++h) {
       double* o = &out[((int64_t)r * Hq + h) * Dv];
@@ -246,8 +252,7 @@ int oracle_sparse_attn(int batch, int bs, int num_blocks, int max_blocks,
       double m = -INFINITY;
       for (int j = 0; j < n; ++j) {
         double dot = 0.0;
-        const uint16_t* kr = k_pool + rows[j] * k_row_stride;
-        for (int d = 0; d < Dqk; ++d) dot += qh[d] * or_dec_bf16(kr[d]);
+        for (int d = 0; d < Dqk; ++d) dot += qh[d] * kk[(int64_t)j * Dqk + d];
         z[j] = sm_scale * dot;
         if (z[j] > m) m = z[j];
       }
@@ -255,14 +260,14 @@ int oracle_sparse_attn(int batch, int bs, int num_blocks, int max_blocks,
       for (int j = 0; j < n; ++j) {
         double e = exp(z[j] - m);
         l += e;
-        const uint16_t* vr = v_pool + rows[j] * v_row_stride;
-        for (int d = 0; d < Dv; ++d) o[d] += e * or_dec_bf16(vr[d]);
+        for (int d = 0; d < Dv; ++d) o[d] += e * vv[(int64_t)j * Dv + d];
       }
       for (int d = 0; d < Dv; ++d) o[d] /= l;
       if (lse) lse[(int64_t)r * Hq + h] = m + log(l);
     }
   }
-  free(rows);
+  free(kk);
+  free(vv);
   free(z);
   free(qh);
   return rc;
