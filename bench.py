@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Throughput of the DSA sparse-attention hot path on GB300.
+
+A step is one pass of the path over one batch of synthetic input:
+  decode workloads : index score -> top-K -> sparse attention (decode)
+  prefill workload : index score -> top-K -> sparse attention (prefill)
+The default workload is "dec-batch" (32 sequences, L ~ U[8192, 32768], latent
+64x576 KV, FP8 indexer, top-K 2048); its metric is decode queries/s.  The
+prefill workload (16384 tokens, same shapes) is measured in the same run and
+reported under "prefill" (tokens/s) unless --secondary is empty.
+
+Timing: W untimed warm-up steps, then K timed steps; before each timed step a
+512 MiB buffer is written to flush L2 (outside the timed region); each step is
+bracketed by CUDA events on the stream the kernels are launched on, with a
+barrier and a synchronize on both sides of the timed loop; the reported time is
+the max over ranks.  With N GPUs (torchrun) every rank runs its own batch
+(weak scaling, no data-path collective).
+
+--impl reference times the CPU oracle (test infrastructure, one thread) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ helpers --
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_attention_score_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_files):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_sha(src_files):
+        return None
+    return e.get("traffic_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- workloads --
+def workload_case(name, rank):
+    import workloads as W
+    # weak scaling: every rank draws its own batch
+    seeds = {"dec-tiny": 0, "dec-batch": 1, "prefill": 2, "long-dec": 3, "million": 4}
+    return W.config(name, seed=seeds[name] + 1000 * rank)
+
+
+def algorithmic(case):
+    """Algorithmic bytes / flops of one step (indexer keys + gathered KV rows for
+    decode; tensor flops for prefill)."""
+    elt_i = 1 if case.idx_dtype == "fp8" else 2
+    sel = np.minimum(case.n_elig.astype(np.int64), case.K)
+    kv_row = case.Dkv * 2 if case.latent else (case.Dqk + case.Dv) * 2
+    idx_bytes = int(case.n_elig.astype(np.int64).sum()) * case.D_i * elt_i
+    if case.kind == "decode":
+        idx_bytes = int(case.seq_lens.astype(np.int64).sum()) * case.D_i * elt_i
+    gather_bytes = int(sel.sum()) * kv_row
+    idx_flops = 2.0 * float(case.n_elig.astype(np.int64).sum()) * case.H_i * case.D_i
+    attn_flops = 2.0 * float(sel.sum()) * case.Hq * (case.Dqk + case.Dv)
+    return dict(index_bytes=idx_bytes, gather_bytes=gather_bytes, index_flops=idx_flops,
+                attn_flops=attn_flops)
+
+
+# ----------------------------------------------------------------- GPU arm --
+def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
+    import torch
+
+    import sparse_attention_score_gb300 as dsa
+    from workloads import device as wdev
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    case = workload_case(name, rank)
+    d = wdev.upload(case, dev)
+    layout = wdev.layout_of(case, d)
+    kind = case.kind
+    pipe = dsa.Pipeline(layout, kind=kind, Nq=case.Nq, Hq=case.Hq, Dqk=case.Dqk, Dv=case.Dv,
+                        H_i=case.H_i, D_i=case.D_i, K=case.K, device=dev)
+    qs = None if kind == "decode" else d.q_seq
+    qp = None if kind == "decode" else d.q_pos
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        dsa.index_score(layout, d.q_idx, d.w, d.kidx_pool, pipe.scores, pipe.ws_index, q_seq=qs,
+                        q_pos=qp)
+        if evs:
+            evs[1].record(stream)
+        dsa.topk(pipe.scores, d.n_elig, case.K, pipe.idx, pipe.ws_topk)
+        if evs:
+            evs[2].record(stream)
+        if kind == "decode":
+            dsa.sparse_attn_decode(layout, d.q, d.k_pool, d.v_pool, pipe.idx, case.sm_scale,
+                                   pipe.out, pipe.lse, pipe.ws_attn)
+        else:
+            dsa.sparse_attn_prefill(layout, d.q, d.k_pool, d.v_pool, pipe.idx, case.sm_scale,
+                                    pipe.out, pipe.lse, pipe.ws_attn, q_seq=d.q_seq)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    n0 = dsa.launch_count()
+    for i in range(steps):
+        flush.fill_(float(i))
+        step(evs[i])
+    torch.cuda.synchronize()
+    launches = dsa.launch_count() - n0
+    clocks = sampler.stop()
+    per = np.array([[evs[i][0].elapsed_time(evs[i][k]) for k in (1, 2, 3)] for i in range(steps)])
+    stage = np.diff(np.concatenate([np.zeros((steps, 1)), per], axis=1), axis=1)  # ms per stage
+    total_ms = float(per[:, 2].sum())
+    status = pipe.status()
+
+    e2e = None
+    if do_e2e:
+        e2e = run_e2e(case, d, pipe, layout, steps, warmup, dev, dsa, flush)
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
+                launches=int(launches), clocks=clocks, status=status, e2e=e2e)
+
+
+def run_e2e(case, d, pipe, layout, steps, warmup, dev, dsa, flush):
+    """Same step through the public API with host buffers: H2D of the step's
+    inputs (queries, indexer queries, weights, block table, lengths) from pinned
+    memory, the three stages, D2H of the attention output."""
+    import torch
+    host = {
+        "q": torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "q_idx": (torch.from_numpy(case.q_idx.view(np.int16)).view(torch.bfloat16)
+                  if case.idx_dtype == "bf16" else torch.from_numpy(case.q_idx)).pin_memory(),
+        "w": torch.from_numpy(case.w).pin_memory(),
+        "block_table": torch.from_numpy(case.block_table).pin_memory(),
+        "seq_lens": torch.from_numpy(case.seq_lens).pin_memory(),
+    }
+    out_host = torch.empty(pipe.out.shape, dtype=pipe.out.dtype).pin_memory()
+    dst = {"q": d.q, "q_idx": d.q_idx, "w": d.w, "block_table": d.block_table,
+           "seq_lens": d.seq_lens}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k, t in host.items():
+            dst[k].copy_(t, non_blocking=True)
+        pipe.run(d.q, d.q_idx, d.w, d.kidx_pool, d.k_pool, d.v_pool, case.sm_scale,
+                 n_eligible=d.n_elig if case.kind != "decode" else None,
+                 q_seq=None if case.kind == "decode" else d.q_seq,
+                 q_pos=None if case.kind == "decode" else d.q_pos)
+        out_host.copy_(pipe.out, non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        step()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(2.0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    units = case.Nq if case.kind == "prefill" else case.B
+    return {"value": units * steps / (tot / 1e3), "unit": unit_of(case),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def unit_of(case):
+    return "tokens/s" if case.kind == "prefill" else "queries/s"
+
+
+def metric_of(case):
+    return "prefill tokens/sec" if case.kind == "prefill" else "decode queries/sec"
+
+
+def roofline_of(res, peaks):
+    """Roofline of the dominant kernel and of the whole step."""
+    case = res["case"]
+    alg = algorithmic(case)
+    st = res["stage_ms"]  # [index, topk, attn] ms per step (avg)
+    if case.kind == "decode":
+        cands = {
+            "index_score": (alg["index_bytes"], st[0], ["index_score.cu"]),
+            "sparse_attn": (alg["gather_bytes"], st[2], ["attn.cu"]),
+        }
+        dom = max(cands, key=lambda k: cands[k][1])
+        nbytes, ms, srcs = cands[dom]
+        ach = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic(f"{dom}:{case.name}", srcs),
+                "peak_source": peaks["source"]}
+        step_bytes = alg["index_bytes"] + alg["gather_bytes"]
+        step_ms = res["total_ms"] / max(1, len(res.get("_steps", [1])))
+        return roof, step_bytes
+    cands = {
+        "index_score": (alg["index_flops"], st[0], ["index_score.cu"]),
+        "sparse_attn": (alg["attn_flops"], st[2], ["attn.cu"]),
+    }
+    dom = max(cands, key=lambda k: cands[k][1])
+    fl, ms, srcs = cands[dom]
+    ach = fl / (ms / 1e3) / 1e12
+    # FP8 indexer: the bf16 peak times the nominal fp8/bf16 ratio of 2
+    peak = peaks["bf16_tflops"] * (2.0 if (dom == "index_score" and case.idx_dtype == "fp8") else 1.0)
+    roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 2), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "traffic": ncu_traffic(f"{dom}:{case.name}", srcs), "peak_source": peaks["source"]}
+    return roof, alg["index_flops"] + alg["attn_flops"]
+
+
+# ---------------------------------------------------------------- CPU oracle --
+def oracle_sample(case, budget_s=15.0, max_units=None):
+    """Run the oracle over queries of the case until the budget is spent; returns
+    (units processed, seconds)."""
+    import oracle
+    code = oracle.BF16 if case.idx_dtype == "bf16" else oracle.FP8_E4M3
+    t0 = time.perf_counter()
+    done = 0
+    order = np.arange(case.Nq)
+    if case.kind == "prefill":
+        order = np.random.default_rng(0).permutation(case.Nq)
+    for r in order:
+        rr = np.array([r])
+        s = oracle.index_score(case.block_table, case.seq_lens, case.bs, case.num_blocks,
+                               case.q_seq[rr], case.q_pos[rr], case.q_idx[rr], case.w[rr],
+                               case.kidx_pool, code, int(case.n_elig[r]))
+        idx = oracle.topk(s, case.n_elig[rr], case.K)
+        oracle.sparse_attn(case.block_table, case.seq_lens, case.bs, case.num_blocks,
+                           case.q_seq[rr], case.q[rr], case.k_pool, case.v_pool, idx,
+                           case.sm_scale, Dv=case.Dv)
+        done += 1
+        if time.perf_counter() - t0 > budget_s or (max_units and done >= max_units):
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(case, budget_s):
+    n, t = oracle_sample(case, budget_s)
+    return {"value": n / t, "unit": unit_of(case), "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {case.Nq} queries of {case.name} (all three stages, fp64 C oracle, "
+                      f"{t:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    case = workload_case(args.workload, 0)
+    per_step_budget = max(1.0, args.ref_step_seconds)
+    for _ in range(args.warmup):
+        oracle_sample(case, per_step_budget, max_units=1)
+    units, secs = 0, 0.0
+    for _ in range(args.steps):
+        n, t = oracle_sample(case, per_step_budget)
+        units += n
+        secs += t
+    val = units / secs
+    line = {
+        "impl": "reference", "metric": metric_of(case), "value": val, "unit": unit_of(case),
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "queries_per_step_sampled": units / args.steps},
+        "cpu_baseline": {"value": val, "unit": unit_of(case), "cores": 1, "kind": "oracle",
+                         "sample": f"{units} queries of {case.name} over {args.steps} steps"},
+        "e2e": {"value": val, "unit": unit_of(case), "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- main --
+def config_of(case, world):
+    c = {"workload": case.name, "batch": case.B, "queries": case.Nq,
+         "seq_lens": ("U[8192,32768]" if case.name == "dec-batch" else
+                      sorted(set(int(x) for x in case.seq_lens))[:8]),
+         "heads": case.Hq, "dqk": case.Dqk, "dv": case.Dv, "latent": case.latent,
+         "indexer": f"{case.H_i}x{case.D_i} {case.idx_dtype}", "top_k": case.K,
+         "block_size": case.bs, "l2": "flushed: 512 MiB write before every timed step",
+         "parallelism": f"replicas{world}" if world > 1 else "1gpu"}
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dec-batch",
+                    choices=["dec-tiny", "dec-batch", "prefill", "long-dec", "million"])
+    ap.add_argument("--secondary", default="prefill",
+                    help="comma-separated extra workloads reported in the same line")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+
+    peaks = measured_peaks()
+    res = run_gpu(args.workload, args.steps, args.warmup, rank, world, local_rank,
+                  do_e2e=not args.no_e2e)
+    case = res["case"]
+    units = (case.Nq if case.kind == "prefill" else case.B) * world
+    value = units * args.steps / (res["total_ms"] / 1e3)
+    roof, step_work = roofline_of(res, peaks)
+    ms_step = res["total_ms"] / args.steps
+    line = {
+        "metric": metric_of(case), "value": value, "unit": unit_of(case), "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16+" + ("fp8" if case.idx_dtype == "fp8" else "bf16") + " (fp32 accumulate)",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": config_of(case, world),
+        "roofline": roof,
+        "stage_ms": {"index_score": res["stage_ms"][0], "topk": res["stage_ms"][1],
+                     "sparse_attn": res["stage_ms"][2]},
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+        "device_status": res["status"],
+    }
+    if case.kind == "decode":
+        frac = step_work / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
+        line["path_roofline"] = {"bound": "hbm", "algorithmic_bytes_per_step": step_work,
+                                 "frac": round(frac, 4), "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s"}
+    extra = [w for w in args.secondary.split(",") if w and w != args.workload]
+    for wname in extra:
+        r2 = run_gpu(wname, max(3, args.steps // 4), args.warmup, rank, world, local_rank,
+                     do_e2e=False)
+        c2 = r2["case"]
+        u2 = (c2.Nq if c2.kind == "prefill" else c2.B) * world
+        st2 = max(3, args.steps // 4)
+        roof2, work2 = roofline_of(r2, peaks)
+        sub = {"metric": metric_of(c2), "value": u2 * st2 / (r2["total_ms"] / 1e3),
+               "unit": unit_of(c2), "ms_per_step": r2["total_ms"] / st2, "steps": st2,
+               "config": config_of(c2, world), "roofline": roof2,
+               "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
+               "gpu_launches": r2["launches"], "clocks": r2["clocks"]}
+        if c2.kind == "prefill":
+            ideal_s = (algorithmic(c2)["index_flops"] / (peaks["bf16_tflops"] * 2e12) +
+                       algorithmic(c2)["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
+            sub["path_roofline"] = {"bound": "tensor", "frac": round(
+                ideal_s / (r2["total_ms"] / st2 / 1e3), 4)}
+        line[wname.replace("-", "_")] = sub
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,213 @@
+/*
+ * dsa.h -- C ABI of the DSA sparse-attention hot path on GB300 (sm_103a).
+ *
+ * The path has three stages over a block-paged KV cache:
+ *   1. indexer score  -- "Day-0 Adaptation of Trillion-Parameter MoE Models on
+ *      Domestic GPUs", section 3 (1) Index Selection: a lightweight similarity
+ *      score of every cached position against the query;
+ *   2. top-K          -- same passage ("block-wise scoring + intra-block
+ *      reduction + cross-block merge"), with the deterministic tie rule of
+ *      "Day-0 Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
+ *      Accelerators", section 4 (equal scores: the lower position wins);
+ *   3. sparse attention -- first page, section 3 (3): exact softmax attention
+ *      over the selected positions only, with separate decode (memory-bound)
+ *      and prefill (compute-bound) paths.
+ * The cache layout follows first page, section 3 (2): pages of `block_size`
+ * consecutive positions stored contiguously, an index table jumping between
+ * pages.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or keeps a pointer after a call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and launches kernels only: no host synchronisation, no
+ *    allocation, so the calls may be captured into a CUDA graph.
+ *  - Tensors are dense and row-major in the shapes written next to them, except
+ *    the KV pools, whose rows are `*_row_stride` elements apart.
+ *  - Return value: DSA_OK, or a negative DSA_ERR_* code for errors the host can
+ *    see (bad pointer, shape, dtype or workspace).  Then nothing was launched
+ *    and the message is in dsa_last_error_string().
+ *  - Errors that depend on device data (a block-table entry outside
+ *    [0, num_blocks), an index past its sequence, a bounded wait that ran out)
+ *    never trap: the offending position or row is skipped (score -inf, row left
+ *    out of the softmax) and a DSA_STATUS_* bit is OR-ed into the status word
+ *    at the start of the call's workspace; dsa_get_status() reads it.
+ *  - Workspaces: query the size with the matching dsa_*_workspace_size(), pass a
+ *    caller-owned device buffer of at least that size, 256-byte aligned and
+ *    ZERO-FILLED before its first use.  The library leaves it in a reusable
+ *    state after every call (counters return to zero; the status word is sticky
+ *    until read with clear=1).  Calls that share a workspace must not overlap
+ *    on the GPU (issue them on one stream, or order the streams).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* = cudaStream_t */
+
+/* host-visible return codes */
+#define DSA_OK 0
+#define DSA_ERR_INVALID (-1)     /* null pointer, bad shape, K, stride or layout */
+#define DSA_ERR_UNSUPPORTED (-2) /* no kernel for this dtype / head count / dims */
+#define DSA_ERR_WORKSPACE (-3)   /* workspace missing, misaligned or too small */
+#define DSA_ERR_CUDA (-4)        /* a CUDA call failed; see dsa_last_error_string() */
+#define DSA_ERR_TIMEOUT (-5)     /* reported by dsa_get_status() users, see below */
+
+/* device status bits (dsa_get_status) */
+#define DSA_STATUS_BAD_BLOCK 0x1  /* block-table entry outside [0, num_blocks) */
+#define DSA_STATUS_BAD_INDEX 0x2  /* selected index >= its sequence length */
+#define DSA_STATUS_BAD_LENGTH 0x4 /* seq_len > max_blocks_per_seq*block_size, or > ld */
+#define DSA_STATUS_TIMEOUT 0x8    /* a bounded device wait gave up */
+
+/* element types */
+#define DSA_BF16 0     /* bfloat16 */
+#define DSA_FP8_E4M3 1 /* OCP FP8 E4M3 ("fn": no infinities) */
+
+/*
+ * Paged cache layout ("Day-0 Adaptation of Trillion-Parameter MoE Models on
+ * Domestic GPUs", section 3 (2)).  Logical position p of sequence b is stored
+ * in physical row  block_table[b][p / block_size] * block_size + p % block_size
+ * of every pool (KV pool, indexer-key pool).  Unused table entries may hold
+ * any value; they are never read.
+ */
+typedef struct dsa_paged_layout {
+  int32_t block_size;          /* positions per page, 1..1024 (64 in the workloads) */
+  int32_t num_blocks;          /* pages in each pool (NB) */
+  int32_t max_blocks_per_seq;  /* row length of block_table */
+  int32_t batch;               /* number of sequences B */
+  int32_t max_seq_len;         /* host-known bound: every seq_lens[b] <= max_seq_len */
+  int32_t reserved_;           /* set to 0 */
+  const int32_t* block_table;  /* device [batch][max_blocks_per_seq] */
+  const int32_t* seq_lens;     /* device [batch]: cached positions L_b (query included) */
+} dsa_paged_layout;
+
+/* ---------------------------------------------------------------------------
+ * Stage 1: indexer score.
+ * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
+ * section 3 (1) ("similarity scoring" of historical positions), read as
+ *     scores[r][p] = sum_h w[r][h] * max(0, sum_d q_idx[r][h][d] * k_idx[p][d])
+ * for every position p the query may see: p <= q_pos[r] and p < L_b (causal,
+ * the current position included).  Every other entry of the row up to ld is
+ * written as -inf.  Accumulation is fp32; with integer-valued q_idx/k_idx/w
+ * (the pages' workloads) the scores are exact integers below 2^24.
+ *
+ *  layout      paged layout; only block_table/seq_lens rows of the queried
+ *              sequences are read
+ *  q_idx       [Nq][H_i][D_i] of `dtype` -- indexer queries
+ *  w           [Nq][H_i] fp32 -- head weights
+ *  kidx_pool   [num_blocks][block_size][D_i] of `dtype` -- indexer keys
+ *  dtype       DSA_BF16 or DSA_FP8_E4M3 (q_idx and kidx_pool share it)
+ *  H_i, D_i    indexer heads (1..128) and dim (32, 64 or 128)
+ *  q_seq       [Nq] sequence of each query, or NULL: query r is sequence r
+ *  q_pos       [Nq] absolute position of each query, or NULL: L_b - 1 (decode)
+ *  scores      [Nq][ld] fp32 output; ld >= max eligible positions of a row
+ *  ws          workspace of dsa_index_score_workspace_size() bytes
+ * Errors: DSA_ERR_INVALID for null pointers, Nq < 0, ld < 1 or a bad layout;
+ * DSA_ERR_UNSUPPORTED for other H_i/D_i/dtype.  Device: out-of-range block ids
+ * give -inf scores and DSA_STATUS_BAD_BLOCK.
+ */
+size_t dsa_index_score_workspace_size(int Nq, int H_i, int D_i, int64_t ld);
+int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                    const void* kidx_pool, int dtype, int H_i, int D_i,
+                    const int32_t* q_seq, const int32_t* q_pos, int Nq, float* scores,
+                    int64_t ld, void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Stage 2: top-K selection.
+ * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
+ * section 3 (1) (Top-K filtering as block-wise scoring, intra-block reduction
+ * and cross-block merge, without a global sort); tie rule from "Day-0
+ * Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
+ * Accelerators", section 4: among equal scores the lower position wins.
+ * For row r, among positions 0..n_eligible[r]-1, keep the min(K, n) positions
+ * with the largest score (scores compared as values: -0.0 ties +0.0), write
+ * them to idx[r] in ascending position order and pad with -1.
+ *
+ *  scores      [Nq][ld] fp32 (finite or -inf; NaN ranks below every value)
+ *  n_eligible  [Nq] int32, each in [0, ld] (larger values are clamped to ld
+ *              and flagged DSA_STATUS_BAD_LENGTH)
+ *  K           1..65536
+ *  idx         [Nq][K] int32 output
+ *  ws          workspace of dsa_topk_workspace_size() bytes
+ */
+size_t dsa_topk_workspace_size(int Nq, int64_t ld, int K);
+int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
+             int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Stage 3a: sparse attention, decode (one query per sequence).
+ * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
+ * section 3 (3) (decode: one token per step, memory-bandwidth-bound) and the
+ * execution chain of "Day-0 Adaptation of Ultra-Large-Scale MoE Models on
+ * Heterogeneous AI Accelerators", section 4 (cache gather + sparse attention).
+ * For sequence b and head h, over the selected positions j (idx[b][*] >= 0),
+ * whose rows are gathered through the block table:
+ *     z_j = sm_scale * q[b][h] . K_j,   out[b][h] = sum_j softmax(z)_j V_j,
+ *     lse[b][h] = log sum_j exp(z_j)
+ * One shared K/V head (multi-query); fp32 accumulation and softmax.
+ *
+ *  q            [B][Hq][Dqk] bf16
+ *  k_pool       physical rows of Dqk bf16, k_row_stride elements apart
+ *  v_pool       physical rows of Dv bf16, v_row_stride elements apart; may be
+ *               k_pool itself (latent cache: V = first Dv dims of the K row)
+ *  Hq           1..128 query heads; Dqk, Dv multiples of 8, <= 1024
+ *  idx          [B][K] int32 positions from dsa_topk (-1 = padding, skipped)
+ *  out          [B][Hq][Dv] bf16 output (0 for a row with no selected position)
+ *  lse          [B][Hq] fp32 output, or NULL (-inf for an empty row)
+ *  ws           workspace of dsa_sparse_attn_decode_workspace_size() bytes
+ * Device errors: an index >= L_b or a bad block id skips that row and sets
+ * DSA_STATUS_BAD_INDEX / DSA_STATUS_BAD_BLOCK.
+ */
+size_t dsa_sparse_attn_decode_workspace_size(int B, int Hq, int Dqk, int Dv, int K);
+int dsa_sparse_attn_decode(const dsa_paged_layout* layout, const void* q, const void* k_pool,
+                           int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
+                           int Hq, int Dqk, int Dv, const int32_t* idx, int K, float sm_scale,
+                           void* out, float* lse, void* ws, size_t ws_bytes,
+                           dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Stage 3b: sparse attention, prefill (many queries, each with its own
+ * selected set).  Source: "Day-0 Adaptation of Trillion-Parameter MoE Models
+ * on Domestic GPUs", section 3 (3) (prefill: whole prompt at once,
+ * compute-intensive).  Same arithmetic as stage 3a for each query r of
+ * sequence q_seq[r]:
+ *  q            [Nq][Hq][Dqk] bf16
+ *  q_seq        [Nq] int32 sequence of each query, or NULL: all in sequence 0
+ *  idx          [Nq][K] int32
+ *  out          [Nq][Hq][Dv] bf16, lse [Nq][Hq] fp32 or NULL
+ *  ws           workspace of dsa_sparse_attn_prefill_workspace_size() bytes
+ * Other arguments and errors as for stage 3a.
+ */
+size_t dsa_sparse_attn_prefill_workspace_size(int Nq, int Hq, int Dqk, int Dv, int K);
+int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const void* k_pool,
+                            int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
+                            int Hq, int Dqk, int Dv, const int32_t* q_seq, int Nq,
+                            const int32_t* idx, int K, float sm_scale, void* out, float* lse,
+                            void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Utilities (no counterpart on the pages).
+ * dsa_get_status: copy the status word of a workspace to *status (host), after
+ *   the work queued on `stream` so far has finished (this call synchronises the
+ *   stream); clear != 0 resets it to 0.  Returns DSA_OK or DSA_ERR_*.
+ * dsa_last_error_string: message of the last failing call on this host thread.
+ * dsa_launch_count: kernels this library has launched in this process.
+ * dsa_version: 10000*major + 100*minor + patch.
+ */
+int dsa_get_status(void* ws, dsa_stream_t stream, int32_t* status, int clear);
+const char* dsa_last_error_string(void);
+uint64_t dsa_launch_count(void);
+int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

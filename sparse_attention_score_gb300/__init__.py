@@ -1,0 +1,269 @@
+"""Python binding of libdsa.so -- the DSA sparse-attention hot path for GB300.
+
+Argument marshalling only: every stage runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current CUDA stream; tensors are passed
+as raw device pointers to the C ABI declared in ``include/dsa.h``.
+
+Stages (names as in the C ABI):
+
+* :func:`index_score` -- indexer score of every cached position, ReLU-weighted
+  over indexer heads ("Day-0 Adaptation of Trillion-Parameter MoE Models on
+  Domestic GPUs", section 3 (1));
+* :func:`topk` -- exact top-K per query, ties to the lower position ("Day-0
+  Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
+  Accelerators", section 4);
+* :func:`sparse_attn_decode` / :func:`sparse_attn_prefill` -- exact softmax
+  attention over the selected rows gathered through the block table (first
+  page, section 3 (2)-(3)).
+
+:func:`decode` and :func:`prefill` chain the three stages with workspaces
+allocated through torch.  There is no CPU fallback: importing this package
+raises if ``libdsa.so`` has not been built, and every call raises
+:class:`DsaError` if the library reports an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa.so")
+
+DSA_OK = 0
+DSA_BF16 = 0
+DSA_FP8_E4M3 = 1
+STATUS_BAD_BLOCK = 0x1
+STATUS_BAD_INDEX = 0x2
+STATUS_BAD_LENGTH = 0x4
+STATUS_TIMEOUT = 0x8
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = _lib.dsa_last_error_string().decode(errors="replace")
+        super().__init__(f"{where} failed with code {code}: {msg}")
+        self.code = code
+
+
+class PagedLayoutC(ctypes.Structure):
+    _fields_ = [("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("reserved_", ctypes.c_int32),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p)]
+
+
+_vp, _i, _i64, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_LP = ctypes.POINTER(PagedLayoutC)
+
+
+def _sig(name, restype, argtypes):
+    fn = getattr(_lib, name)
+    fn.restype = restype
+    fn.argtypes = argtypes
+    return fn
+
+
+_sig("dsa_version", _i, [])
+_sig("dsa_launch_count", ctypes.c_uint64, [])
+_sig("dsa_last_error_string", ctypes.c_char_p, [])
+_sig("dsa_get_status", _i, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), _i])
+_sig("dsa_index_score_workspace_size", _sz, [_i, _i, _i, _i64])
+_sig("dsa_index_score", _i, [_LP, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _i64, _vp, _sz, _vp])
+_sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
+_sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
+_sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
+_sig("dsa_sparse_attn_decode", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _f, _vp,
+                                    _vp, _vp, _sz, _vp])
+_sig("dsa_sparse_attn_prefill_workspace_size", _sz, [_i, _i, _i, _i, _i])
+_sig("dsa_sparse_attn_prefill", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _vp, _i,
+                                     _f, _vp, _vp, _vp, _sz, _vp])
+
+SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_status",
+           "dsa_index_score_workspace_size", "dsa_index_score", "dsa_topk_workspace_size",
+           "dsa_topk", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
+           "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def version() -> int:
+    return int(_lib.dsa_version())
+
+
+def launch_count() -> int:
+    """Kernels launched by libdsa.so in this process so far."""
+    return int(_lib.dsa_launch_count())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != DSA_OK:
+        raise DsaError(rc, where)
+
+
+def _elt_dtype(t: torch.Tensor) -> int:
+    return DSA_FP8_E4M3 if t.element_size() == 1 else DSA_BF16
+
+
+@dataclass
+class PagedLayout:
+    """Block table + sequence lengths on the device (tensors kept alive here)."""
+
+    block_table: torch.Tensor  # int32 [B, max_blocks]
+    seq_lens: torch.Tensor     # int32 [B]
+    block_size: int
+    num_blocks: int
+    max_seq_len: int
+
+    def __post_init__(self):
+        if self.block_table.dtype != torch.int32 or self.seq_lens.dtype != torch.int32:
+            raise TypeError("block_table and seq_lens must be int32")
+        self._c = PagedLayoutC(int(self.block_size), int(self.num_blocks),
+                               int(self.block_table.shape[1]), int(self.block_table.shape[0]),
+                               int(self.max_seq_len), 0, self.block_table.data_ptr(),
+                               self.seq_lens.data_ptr())
+
+    @property
+    def batch(self) -> int:
+        return int(self.block_table.shape[0])
+
+    def c(self):
+        return ctypes.byref(self._c)
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zero-filled device workspace (uint8), 256-byte aligned by the allocator."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def index_score_workspace_size(Nq, H_i, D_i, ld) -> int:
+    return int(_lib.dsa_index_score_workspace_size(Nq, H_i, D_i, ld))
+
+
+def topk_workspace_size(Nq, ld, K) -> int:
+    return int(_lib.dsa_topk_workspace_size(Nq, ld, K))
+
+
+def sparse_attn_decode_workspace_size(B, Hq, Dqk, Dv, K) -> int:
+    return int(_lib.dsa_sparse_attn_decode_workspace_size(B, Hq, Dqk, Dv, K))
+
+
+def sparse_attn_prefill_workspace_size(Nq, Hq, Dqk, Dv, K) -> int:
+    return int(_lib.dsa_sparse_attn_prefill_workspace_size(Nq, Hq, Dqk, Dv, K))
+
+
+def index_score(layout: PagedLayout, q_idx, w, kidx_pool, scores, ws, q_seq=None, q_pos=None,
+                stream=None):
+    """scores[Nq, ld] <- indexer scores (see include/dsa.h, dsa_index_score)."""
+    Nq, H_i, D_i = q_idx.shape
+    rc = _lib.dsa_index_score(layout.c(), _ptr(q_idx), _ptr(w), _ptr(kidx_pool),
+                              _elt_dtype(kidx_pool), H_i, D_i, _ptr(q_seq), _ptr(q_pos), Nq,
+                              _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "dsa_index_score")
+
+
+def topk(scores, n_eligible, K, idx, ws, stream=None):
+    """idx[Nq, K] <- top-K positions, ascending, -1 padded."""
+    Nq, ld = scores.shape
+    rc = _lib.dsa_topk(_ptr(scores), ld, _ptr(n_eligible), Nq, K, _ptr(idx), _ptr(ws), ws.numel(),
+                       _stream(stream))
+    _check(rc, "dsa_topk")
+
+
+def sparse_attn_decode(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
+                       stream=None):
+    B, Hq, Dqk = q.shape
+    Dv = out.shape[2]
+    rc = _lib.dsa_sparse_attn_decode(layout.c(), _ptr(q), _ptr(k_pool), k_pool.shape[-1],
+                                     _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(idx),
+                                     idx.shape[1], float(sm_scale), _ptr(out), _ptr(lse), _ptr(ws),
+                                     ws.numel(), _stream(stream))
+    _check(rc, "dsa_sparse_attn_decode")
+
+
+def sparse_attn_prefill(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
+                        q_seq=None, stream=None):
+    Nq, Hq, Dqk = q.shape
+    Dv = out.shape[2]
+    rc = _lib.dsa_sparse_attn_prefill(layout.c(), _ptr(q), _ptr(k_pool), k_pool.shape[-1],
+                                      _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(q_seq), Nq,
+                                      _ptr(idx), idx.shape[1], float(sm_scale), _ptr(out),
+                                      _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "dsa_sparse_attn_prefill")
+
+
+def get_status(ws, clear: bool = True, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check(_lib.dsa_get_status(_ptr(ws), _stream(stream), ctypes.byref(v), int(clear)),
+           "dsa_get_status")
+    return int(v.value)
+
+
+class Pipeline:
+    """The three stages of one decode or prefill step with preallocated buffers.
+
+    kind="decode": one query per sequence at position L_b - 1 (q [B, Hq, Dqk]).
+    kind="prefill": Nq queries with explicit q_seq / q_pos.
+    Buffers (scores, idx, out, lse, workspaces) are allocated once through torch.
+    """
+
+    def __init__(self, layout: PagedLayout, *, kind: str, Nq: int, Hq: int, Dqk: int, Dv: int,
+                 H_i: int, D_i: int, K: int, ld: Optional[int] = None, device="cuda"):
+        self.layout, self.kind, self.K = layout, kind, int(K)
+        self.Nq, self.Hq, self.Dqk, self.Dv = int(Nq), int(Hq), int(Dqk), int(Dv)
+        self.ld = int(ld if ld is not None else max(layout.max_seq_len, 1))
+        self.scores = torch.empty((self.Nq, self.ld), dtype=torch.float32, device=device)
+        self.idx = torch.empty((self.Nq, self.K), dtype=torch.int32, device=device)
+        self.out = torch.empty((self.Nq, Hq, Dv), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((self.Nq, Hq), dtype=torch.float32, device=device)
+        self.ws_index = workspace(index_score_workspace_size(self.Nq, H_i, D_i, self.ld), device)
+        self.ws_topk = workspace(topk_workspace_size(self.Nq, self.ld, self.K), device)
+        if kind == "decode":
+            n = sparse_attn_decode_workspace_size(self.Nq, Hq, Dqk, Dv, self.K)
+        else:
+            n = sparse_attn_prefill_workspace_size(self.Nq, Hq, Dqk, Dv, self.K)
+        self.ws_attn = workspace(n, device)
+
+    def run(self, q, q_idx, w, kidx_pool, k_pool, v_pool, sm_scale, n_eligible=None, q_seq=None,
+            q_pos=None, stream=None):
+        if n_eligible is None:
+            if self.kind != "decode":
+                raise ValueError("prefill needs n_eligible (q_pos + 1)")
+            n_eligible = self.layout.seq_lens
+        index_score(self.layout, q_idx, w, kidx_pool, self.scores, self.ws_index, q_seq=q_seq,
+                    q_pos=q_pos, stream=stream)
+        topk(self.scores, n_eligible, self.K, self.idx, self.ws_topk, stream=stream)
+        if self.kind == "decode":
+            sparse_attn_decode(self.layout, q, k_pool, v_pool, self.idx, sm_scale, self.out,
+                               self.lse, self.ws_attn, stream=stream)
+        else:
+            sparse_attn_prefill(self.layout, q, k_pool, v_pool, self.idx, sm_scale, self.out,
+                                self.lse, self.ws_attn, q_seq=q_seq, stream=stream)
+        return self.out
+
+    def status(self) -> int:
+        return (get_status(self.ws_index) | get_status(self.ws_topk) | get_status(self.ws_attn))

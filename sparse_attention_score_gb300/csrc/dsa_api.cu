@@ -1,0 +1,220 @@
+// dsa_api.cu -- the C ABI of libdsa.so: argument validation, workspace
+// checks, dispatch to the kernels, error reporting.  Declarations and the
+// contract of every entry point are in include/dsa.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <string>
+
+#include "dsa.h"
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local std::string g_last_error;
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int set_error(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return set_error(DSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+static int check_layout(const dsa_paged_layout* L, LayoutDev* out) {
+  if (!L) return set_error(DSA_ERR_INVALID, "layout is NULL");
+  if (!L->block_table || !L->seq_lens)
+    return set_error(DSA_ERR_INVALID, "layout.block_table / seq_lens is NULL");
+  if (L->block_size < 1 || L->block_size > 1024)
+    return set_error(DSA_ERR_INVALID, "layout.block_size must be in 1..1024");
+  if (L->num_blocks < 1 || L->max_blocks_per_seq < 1 || L->batch < 1)
+    return set_error(DSA_ERR_INVALID, "layout.num_blocks/max_blocks_per_seq/batch must be >= 1");
+  if (L->max_seq_len < 0 ||
+      (long long)L->max_seq_len > (long long)L->max_blocks_per_seq * L->block_size)
+    return set_error(DSA_ERR_INVALID,
+                     "layout.max_seq_len must be in 0..max_blocks_per_seq*block_size");
+  out->bs = L->block_size;
+  out->nb = L->num_blocks;
+  out->maxb = L->max_blocks_per_seq;
+  out->batch = L->batch;
+  out->max_len = L->max_seq_len;
+  out->bt = L->block_table;
+  out->seq_lens = L->seq_lens;
+  return DSA_OK;
+}
+
+static int check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return set_error(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (((uintptr_t)ws) & 255u) return set_error(DSA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  if (have < need)
+    return set_error(DSA_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) +
+                                            " bytes, got " + std::to_string(have));
+  return DSA_OK;
+}
+
+static bool aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+uint64_t dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* dsa_last_error_string(void) { return g_last_error.c_str(); }
+
+int dsa_get_status(void* ws, dsa_stream_t stream, int32_t* status, int clear) {
+  if (!ws || !status) return set_error(DSA_ERR_INVALID, "dsa_get_status: NULL argument");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess)
+    return set_error(DSA_ERR_CUDA, std::string("dsa_get_status: ") + cudaGetErrorString(e));
+  *status = v;
+  return DSA_OK;
+}
+
+size_t dsa_index_score_workspace_size(int Nq, int H_i, int D_i, int64_t ld) {
+  return index_score_ws(Nq, H_i, D_i, (long long)ld);
+}
+
+int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                    const void* kidx_pool, int dtype, int H_i, int D_i, const int32_t* q_seq,
+                    const int32_t* q_pos, int Nq, float* scores, int64_t ld, void* ws,
+                    size_t ws_bytes, dsa_stream_t stream) {
+  IndexParams p{};
+  int rc = check_layout(layout, &p.lay);
+  if (rc) return rc;
+  if (Nq < 0 || ld < 1) return set_error(DSA_ERR_INVALID, "index_score: Nq < 0 or ld < 1");
+  if (Nq > 65535) return set_error(DSA_ERR_UNSUPPORTED, "index_score: Nq > 65535");
+  if (!q_idx || !w || !kidx_pool || !scores)
+    return set_error(DSA_ERR_INVALID, "index_score: NULL tensor pointer");
+  if (!index_score_supported(dtype, H_i, D_i))
+    return set_error(DSA_ERR_UNSUPPORTED,
+                     "index_score: supported dtype BF16/FP8_E4M3, H_i 1..128, D_i 32/64/128");
+  if (!aligned16(q_idx) || !aligned16(kidx_pool))
+    return set_error(DSA_ERR_INVALID, "index_score: q_idx / kidx_pool must be 16-byte aligned");
+  rc = check_ws(ws, ws_bytes, index_score_ws(Nq, H_i, D_i, (long long)ld));
+  if (rc) return rc;
+  p.q_idx = q_idx;
+  p.w = w;
+  p.kidx = kidx_pool;
+  p.dtype = dtype;
+  p.H = H_i;
+  p.D = D_i;
+  p.q_seq = q_seq;
+  p.q_pos = q_pos;
+  p.Nq = Nq;
+  p.scores = scores;
+  p.ld = (long long)ld;
+  p.status = reinterpret_cast<int*>(ws);
+  return launch_index_score(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_topk_workspace_size(int Nq, int64_t ld, int K) {
+  return topk_ws(Nq, (long long)ld, K);
+}
+
+int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
+             int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (Nq < 0 || ld < 1 || K < 1 || K > 65536)
+    return set_error(DSA_ERR_INVALID, "topk: need Nq >= 0, ld >= 1, 1 <= K <= 65536");
+  if (!scores || !n_eligible || !idx) return set_error(DSA_ERR_INVALID, "topk: NULL pointer");
+  int rc = check_ws(ws, ws_bytes, topk_ws(Nq, (long long)ld, K));
+  if (rc) return rc;
+  TopkParams p{};
+  p.scores = scores;
+  p.ld = (long long)ld;
+  p.n_elig = n_eligible;
+  p.Nq = Nq;
+  p.K = K;
+  p.idx = idx;
+  p.status = reinterpret_cast<int*>(ws);
+  return launch_topk(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int attn_common(const dsa_paged_layout* layout, const void* q, const void* k_pool,
+                       int64_t k_row_stride, const void* v_pool, int64_t v_row_stride, int Hq,
+                       int Dqk, int Dv, const int32_t* q_seq, int Nq, const int32_t* idx, int K,
+                       float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                       dsa_stream_t stream, bool decode) {
+  AttnParams p{};
+  int rc = check_layout(layout, &p.lay);
+  if (rc) return rc;
+  if (Nq < 0 || K < 1) return set_error(DSA_ERR_INVALID, "sparse_attn: Nq < 0 or K < 1");
+  if (Nq > 65535) return set_error(DSA_ERR_UNSUPPORTED, "sparse_attn: Nq > 65535");
+  if (!q || !k_pool || !v_pool || !idx || !out)
+    return set_error(DSA_ERR_INVALID, "sparse_attn: NULL tensor pointer");
+  if (k_row_stride < Dqk || v_row_stride < Dv || (k_row_stride % 8) || (v_row_stride % 8))
+    return set_error(DSA_ERR_INVALID,
+                     "sparse_attn: row strides must cover Dqk/Dv and be multiples of 8");
+  if (!attn_supported(Hq, Dqk, Dv))
+    return set_error(DSA_ERR_UNSUPPORTED,
+                     "sparse_attn: supported Hq 1..64, Dqk/Dv multiples of 8, Dv <= 512");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+    return set_error(DSA_ERR_INVALID, "sparse_attn: q / k_pool / v_pool must be 16-byte aligned");
+  if (!(sm_scale > 0.0f) || sm_scale != sm_scale)
+    return set_error(DSA_ERR_INVALID, "sparse_attn: sm_scale must be a positive number");
+  rc = check_ws(ws, ws_bytes, attn_ws(Nq, Hq, Dqk, Dv, K, decode));
+  if (rc) return rc;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.kp = reinterpret_cast<const __nv_bfloat16*>(k_pool);
+  p.ks = (long long)k_row_stride;
+  p.vp = reinterpret_cast<const __nv_bfloat16*>(v_pool);
+  p.vs = (long long)v_row_stride;
+  p.Hq = Hq;
+  p.Dqk = Dqk;
+  p.Dv = Dv;
+  p.q_seq = q_seq;
+  p.seq0 = decode ? 0 : 1;
+  p.Nq = Nq;
+  p.idx = idx;
+  p.K = K;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = reinterpret_cast<int*>(ws);
+  return launch_attn(p, decode, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_sparse_attn_decode_workspace_size(int B, int Hq, int Dqk, int Dv, int K) {
+  return attn_ws(B, Hq, Dqk, Dv, K, true);
+}
+
+int dsa_sparse_attn_decode(const dsa_paged_layout* layout, const void* q, const void* k_pool,
+                           int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
+                           int Hq, int Dqk, int Dv, const int32_t* idx, int K, float sm_scale,
+                           void* out, float* lse, void* ws, size_t ws_bytes,
+                           dsa_stream_t stream) {
+  int B = layout ? layout->batch : 0;
+  return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, nullptr,
+                     B, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, true);
+}
+
+size_t dsa_sparse_attn_prefill_workspace_size(int Nq, int Hq, int Dqk, int Dv, int K) {
+  return attn_ws(Nq, Hq, Dqk, Dv, K, false);
+}
+
+int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const void* k_pool,
+                            int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
+                            int Hq, int Dqk, int Dv, const int32_t* q_seq, int Nq,
+                            const int32_t* idx, int K, float sm_scale, void* out, float* lse,
+                            void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, q_seq,
+                     Nq, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// dsa_internal.cuh -- parameter blocks and launcher declarations shared by the
+// translation units of libdsa.so (never installed, never seen by callers).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <string>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Bytes reserved at the head of every workspace: the status word and small
+// self-resetting counters.
+constexpr size_t kWsHeader = 256;
+
+struct LayoutDev {
+  int bs, nb, maxb, batch, max_len;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+};
+
+struct IndexParams {
+  LayoutDev lay;
+  const void* q_idx;
+  const float* w;
+  const void* kidx;
+  int dtype, H, D;
+  const int32_t* q_seq;
+  const int32_t* q_pos;
+  int Nq;
+  float* scores;
+  long long ld;
+  int* status;
+};
+
+struct TopkParams {
+  const float* scores;
+  long long ld;
+  const int32_t* n_elig;
+  int Nq, K;
+  int32_t* idx;
+  int* status;
+};
+
+struct AttnParams {
+  LayoutDev lay;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kp;
+  long long ks;
+  const __nv_bfloat16* vp;
+  long long vs;
+  int Hq, Dqk, Dv;
+  const int32_t* q_seq;  // NULL: query r is sequence r (decode) / sequence 0 (prefill)
+  int seq0;              // 1: q_seq NULL means every query is in sequence 0
+  int Nq;
+  const int32_t* idx;
+  int K;
+  float scale_log2;  // sm_scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  float* part_o;   // [Nq][S][Hq][Dv] unnormalised partial outputs
+  float* part_ml;  // [Nq][S][Hq][2] (running max in log2 units, sum)
+  int S;           // splits of the K selected rows
+};
+
+// host-side bookkeeping (dsa_api.cu)
+void count_launch(int n = 1);
+int set_error(int code, const std::string& msg);
+int check_launch(const char* what);
+
+// launchers: return DSA_OK / DSA_ERR_*
+int launch_index_score(const IndexParams& p, cudaStream_t s);
+bool index_score_supported(int dtype, int H, int D);
+size_t index_score_ws(int Nq, int H, int D, long long ld);
+
+int launch_topk(const TopkParams& p, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t topk_ws(int Nq, long long ld, int K);
+
+int launch_attn(AttnParams p, bool decode, void* ws, size_t ws_bytes, cudaStream_t s);
+bool attn_supported(int Hq, int Dqk, int Dv);
+size_t attn_ws(int Nq, int Hq, int Dqk, int Dv, int K, bool decode);
+
+}  // namespace dsa

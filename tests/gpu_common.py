@@ -1,0 +1,127 @@
+"""Shared helpers of the GPU parity tests (CUDA path through the C ABI vs the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import device as wdev
+
+# Tolerances on attention outputs against the fp64 oracle (bf16 I/O, fp32
+# accumulation): max-abs 1e-2 and mean-abs 2e-3 on out; lse to 1e-3 absolute.
+OUT_MAX_ABS = 1e-2
+OUT_MEAN_ABS = 2e-3
+LSE_ABS = 1e-3
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def lib():
+    from sparse_attention_score_gb300 import _build
+    _build.build()
+    import sparse_attention_score_gb300 as dsa
+    return dsa
+
+
+def code(case):
+    return oracle.BF16 if case.idx_dtype == "bf16" else oracle.FP8_E4M3
+
+
+def oracle_scores(case, ld=None, rows=None):
+    rows = np.arange(case.Nq) if rows is None else np.asarray(rows)
+    return oracle.index_score(case.block_table, case.seq_lens, case.bs, case.num_blocks,
+                              case.q_seq[rows], case.q_pos[rows], case.q_idx[rows], case.w[rows],
+                              case.kidx_pool, code(case), case.max_len if ld is None else ld)
+
+
+def oracle_attn(case, idx, rows=None):
+    rows = np.arange(case.Nq) if rows is None else np.asarray(rows)
+    return oracle.sparse_attn(case.block_table, case.seq_lens, case.bs, case.num_blocks,
+                              case.q_seq[rows], case.q[rows], case.k_pool, case.v_pool, idx,
+                              case.sm_scale, Dv=case.Dv)
+
+
+class GpuRun:
+    """Runs the three stages of a case on the GPU through the binding."""
+
+    def __init__(self, case, dsa=None, ld=None, device="cuda"):
+        self.dsa = dsa or lib()
+        self.case = case
+        self.d = wdev.upload(case, device)
+        self.layout = wdev.layout_of(case, self.d)
+        kind = "decode" if case.kind == "decode" else "prefill"
+        self.pipe = self.dsa.Pipeline(self.layout, kind=kind, Nq=case.Nq, Hq=case.Hq, Dqk=case.Dqk,
+                                      Dv=case.Dv, H_i=case.H_i, D_i=case.D_i, K=case.K, ld=ld,
+                                      device=device)
+
+    def scores(self):
+        d, p = self.d, self.pipe
+        qs = None if self.case.kind == "decode" else d.q_seq
+        qp = None if self.case.kind == "decode" else d.q_pos
+        self.dsa.index_score(self.layout, d.q_idx, d.w, d.kidx_pool, p.scores, p.ws_index,
+                             q_seq=qs, q_pos=qp)
+        return p.scores
+
+    def topk(self, scores=None, n_elig=None):
+        p = self.pipe
+        s = p.scores if scores is None else scores
+        ne = self.d.n_elig if n_elig is None else n_elig
+        self.dsa.topk(s, ne, self.case.K, p.idx, p.ws_topk)
+        return p.idx
+
+    def attn(self, idx=None):
+        d, p, c = self.d, self.pipe, self.case
+        ix = p.idx if idx is None else idx
+        if c.kind == "decode":
+            self.dsa.sparse_attn_decode(self.layout, d.q, d.k_pool, d.v_pool, ix, c.sm_scale, p.out,
+                                        p.lse, p.ws_attn)
+        else:
+            self.dsa.sparse_attn_prefill(self.layout, d.q, d.k_pool, d.v_pool, ix, c.sm_scale,
+                                         p.out, p.lse, p.ws_attn, q_seq=d.q_seq)
+        return p.out, p.lse
+
+    def all(self):
+        self.scores()
+        self.topk()
+        return self.attn()
+
+    def status(self):
+        return self.pipe.status()
+
+
+def assert_out_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - out_ref)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    assert err.max() <= OUT_MAX_ABS, f"{what}: max-abs {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    if lse_gpu is not None:
+        l = lse_gpu.cpu().numpy().astype(np.float64)
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(l), fin), f"{what}: lse finiteness differs"
+        if fin.any():
+            assert np.abs(l[fin] - lse_ref[fin]).max() <= LSE_ABS, f"{what}: lse"
+    return float(err.max()), float(err.mean())
+
+
+def check_topk_definition(s, n, K, idx):
+    """Validity of a selection against its scores (used where the oracle cannot
+    afford a full row): kept set of size min(K,n), ascending, -1 padded, and the
+    worst kept beats the best dropped under (score desc, position asc)."""
+    s = np.where(s == 0, 0.0, s).astype(np.float32)  # -0 ties +0
+    m = min(K, n)
+    kept = idx[:m].astype(np.int64)
+    assert np.all(idx[m:] == -1)
+    assert np.all(np.diff(kept) > 0) and (m == 0 or (kept[0] >= 0 and kept[-1] < n))
+    if m == 0 or m == n:
+        return
+    keep = np.zeros(n, bool)
+    keep[kept] = True
+    ks = s[:n][keep]
+    dp = np.nonzero(~keep)[0]
+    ds = s[:n][~keep]
+    wk = np.lexsort((-kept, ks))[0]
+    bd = np.lexsort((dp, -ds))[0]
+    assert ks[wk] > ds[bd] or (ks[wk] == ds[bd] and kept[wk] < dp[bd])

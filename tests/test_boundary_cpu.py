@@ -1,0 +1,123 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    from sparse_attention_score_gb300 import _build
+    _build.build()
+    import sparse_attention_score_gb300 as m
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_stage_calls():
+    syms = declared_symbols()
+    for s in ("dsa_index_score", "dsa_topk", "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(dsa):
+    lib = ctypes.CDLL(dsa.LIB_PATH)
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    assert set(declared_symbols()) == set(dsa.SYMBOLS)
+
+
+def test_version_and_sizes(dsa):
+    assert dsa.version() >= 100
+    assert dsa.index_score_workspace_size(32, 64, 128, 32768) >= 256
+    assert dsa.topk_workspace_size(32, 32768, 2048) >= 256
+    assert dsa.sparse_attn_decode_workspace_size(32, 64, 576, 512, 2048) >= 256
+    assert dsa.sparse_attn_prefill_workspace_size(16384, 64, 576, 512, 2048) >= 256
+
+
+def _layout(dsa, **kw):
+    f = dict(block_size=64, num_blocks=16, max_blocks_per_seq=4, batch=2, max_seq_len=200,
+             reserved_=0, block_table=0x10000, seq_lens=0x20000)
+    f.update(kw)
+    return dsa.PagedLayoutC(**{k: v for k, v in f.items()})
+
+
+FAKE = ctypes.c_void_p(0x100000)   # never dereferenced: every call below fails validation
+
+
+def test_index_score_rejects_bad_arguments(dsa):
+    lib = dsa.lib()
+    lay = _layout(dsa)
+    ws_ok = dsa.index_score_workspace_size(2, 4, 64, 256)
+    args = lambda **o: dict(dict(layout=ctypes.byref(lay), q=FAKE, w=FAKE, k=FAKE, dt=0, H=4, D=64,
+                                 qs=None, qp=None, Nq=2, s=FAKE, ld=256, ws=FAKE, wsb=ws_ok,
+                                 st=None), **o)
+
+    def call(**o):
+        a = args(**o)
+        return lib.dsa_index_score(a["layout"], a["q"], a["w"], a["k"], a["dt"], a["H"], a["D"],
+                                   a["qs"], a["qp"], a["Nq"], a["s"], a["ld"], a["ws"], a["wsb"],
+                                   a["st"])
+    assert call(layout=None) == -1
+    assert call(q=None) == -1
+    assert call(ld=0) == -1
+    assert call(Nq=-1) == -1
+    assert call(D=48) == -2
+    assert call(H=0) == -2
+    assert call(dt=7) == -2
+    assert call(ws=None) == -3
+    assert call(wsb=10) == -3
+    assert call(ws=ctypes.c_void_p(0x100010)) == -3
+    bad = _layout(dsa, block_size=0)
+    assert call(layout=ctypes.byref(bad)) == -1
+    bad = _layout(dsa, max_seq_len=4 * 64 + 1)
+    assert call(layout=ctypes.byref(bad)) == -1
+    assert "max_seq_len" in dsa.lib().dsa_last_error_string().decode()
+
+
+def test_topk_rejects_bad_arguments(dsa):
+    lib = dsa.lib()
+    ok = dsa.topk_workspace_size(4, 100, 8)
+    assert lib.dsa_topk(FAKE, 100, FAKE, 4, 0, FAKE, FAKE, ok, None) == -1
+    assert lib.dsa_topk(FAKE, 100, FAKE, 4, 70000, FAKE, FAKE, ok, None) == -1
+    assert lib.dsa_topk(None, 100, FAKE, 4, 8, FAKE, FAKE, ok, None) == -1
+    assert lib.dsa_topk(FAKE, 0, FAKE, 4, 8, FAKE, FAKE, ok, None) == -1
+    assert lib.dsa_topk(FAKE, 100, FAKE, 4, 8, FAKE, None, ok, None) == -3
+
+
+def test_attention_rejects_bad_arguments(dsa):
+    lib = dsa.lib()
+    lay = _layout(dsa)
+    ok = dsa.sparse_attn_decode_workspace_size(2, 16, 128, 128, 64)
+
+    def dec(Hq=16, Dqk=128, Dv=128, ks=128, vs=128, scale=0.1, q=FAKE, ws=FAKE, wsb=ok):
+        return lib.dsa_sparse_attn_decode(ctypes.byref(lay), q, FAKE, ks, FAKE, vs, Hq, Dqk, Dv,
+                                          FAKE, 64, scale, FAKE, None, ws, wsb, None)
+    assert dec(q=None) == -1
+    assert dec(ks=64) == -1
+    assert dec(vs=100) == -1
+    assert dec(scale=0.0) == -1
+    assert dec(scale=float("nan")) == -1
+    assert dec(Hq=0) == -2
+    assert dec(Dqk=100, ks=104) == -2
+    assert dec(wsb=1) == -3
+    assert dec(ws=None) == -3
+    okp = dsa.sparse_attn_prefill_workspace_size(3, 16, 128, 128, 64)
+    assert lib.dsa_sparse_attn_prefill(ctypes.byref(lay), FAKE, FAKE, 128, FAKE, 128, 16, 128,
+                                       128, None, 3, FAKE, 0, 0.1, FAKE, None, FAKE, okp,
+                                       None) == -1
+
+
+def test_get_status_rejects_null(dsa):
+    v = ctypes.c_int32(0)
+    assert dsa.lib().dsa_get_status(None, None, ctypes.byref(v), 0) == -1
