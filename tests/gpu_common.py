@@ -19,8 +19,8 @@ def need_gpu():
 
 
 def lib():
-    from sparse_attention_score_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import sparse_attention_score_gb300 as dsa
     return dsa
 

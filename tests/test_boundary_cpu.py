@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "dsa.h")
 
 @pytest.fixture(scope="module")
 def dsa():
-    from sparse_attention_score_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import sparse_attention_score_gb300 as m
     return m
 
