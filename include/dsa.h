@@ -94,8 +94,9 @@ typedef struct dsa_paged_layout {
  * section 3 (1) ("similarity scoring" of historical positions), read as
  *     scores[r][p] = sum_h w[r][h] * max(0, sum_d q_idx[r][h][d] * k_idx[p][d])
  * for every position p the query may see: p <= q_pos[r] and p < L_b (causal,
- * the current position included).  Every other entry of the row up to ld is
- * written as -inf.  Accumulation is fp32; with integer-valued q_idx/k_idx/w
+ * the current position included).  Entries of the row past the last eligible
+ * position are not part of the result and may be left untouched.
+ * Accumulation is fp32; with integer-valued q_idx/k_idx/w
  * (the pages' workloads) the scores are exact integers below 2^24.
  *
  *  layout      paged layout; only block_table/seq_lens rows of the queried
@@ -107,7 +108,7 @@ typedef struct dsa_paged_layout {
  *  H_i, D_i    indexer heads (1..128) and dim (32, 64 or 128)
  *  q_seq       [Nq] sequence of each query, or NULL: query r is sequence r
  *  q_pos       [Nq] absolute position of each query, or NULL: L_b - 1 (decode)
- *  scores      [Nq][ld] fp32 output; ld >= max eligible positions of a row
+ *  scores      [Nq][ld] fp32 output; ld >= eligible positions of every row
  *  ws          workspace of dsa_index_score_workspace_size() bytes
  * Errors: DSA_ERR_INVALID for null pointers, Nq < 0, ld < 1 or a bad layout;
  * DSA_ERR_UNSUPPORTED for other H_i/D_i/dtype.  Device: out-of-range block ids

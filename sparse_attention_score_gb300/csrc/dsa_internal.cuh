@@ -2,6 +2,7 @@
 // translation units of libdsa.so (never installed, never seen by callers).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -73,8 +74,18 @@ void count_launch(int n = 1);
 int set_error(int code, const std::string& msg);
 int check_launch(const char* what);
 
+// host_tma.cu: 2D TMA map with 128-byte swizzle over rows of `inner_elems`
+// elements (1-byte elements if one_byte, else bf16), rows `row_stride_bytes`
+// apart; box of box_inner x box_rows.
+int make_tmap_2d(CUtensorMap* map, const void* base, bool one_byte, uint64_t inner_elems,
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+int sm_count();
+
 // launchers: return DSA_OK / DSA_ERR_*
 int launch_index_score(const IndexParams& p, cudaStream_t s);
+// tensor-core indexer (FP8 E4M3, H_i = 64, D_i = 128, block size 64)
+bool index_tc_eligible(const IndexParams& p);
+int launch_index_tc(const IndexParams& p, cudaStream_t s);
 bool index_score_supported(int dtype, int H, int D);
 size_t index_score_ws(int Nq, int H, int D, long long ld);
 

@@ -6,8 +6,9 @@
 //     s[r][p] = sum_h w[r][h] * max(0, q_idx[r][h] . k_idx[p])
 // over the causal positions p <= q_pos[r], p < L_b; -inf elsewhere in the row.
 //
-// This file holds the CUDA-core kernel used for every supported shape; it is
-// exact for integer-valued inputs (fp32 accumulation of integers < 2^24).
+// This file holds the CUDA-core kernel, used for every shape the tensor-core
+// kernel (index_tc.cu) does not cover; it is exact for integer-valued inputs
+// (fp32 accumulation of integers < 2^24).
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
 
@@ -134,6 +135,7 @@ size_t index_score_ws(int, int, int, long long) { return kWsHeader; }
 
 int launch_index_score(const IndexParams& p, cudaStream_t s) {
   if (p.Nq == 0) return DSA_OK;
+  if (index_tc_eligible(p)) return launch_index_tc(p, s);
   if (p.dtype == DSA_BF16) {
     if (p.D == 32) return launch_generic<32, DSA_BF16>(p, s);
     if (p.D == 64) return launch_generic<64, DSA_BF16>(p, s);

@@ -91,6 +91,14 @@ class GpuRun:
         return self.pipe.status()
 
 
+def assert_scores_equal(s_gpu, s_ref, n_elig):
+    """Bit-exact on every eligible entry of every row (entries past a row's
+    eligible count are not part of the output contract)."""
+    for r in range(s_ref.shape[0]):
+        n = int(n_elig[r])
+        np.testing.assert_array_equal(s_gpu[r, :n], s_ref[r, :n], err_msg=f"row {r}")
+
+
 def assert_out_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     err = np.abs(o - out_ref)

@@ -11,8 +11,8 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import (GpuRun, assert_out_close, check_topk_definition, need_gpu, oracle_attn,
-                        oracle_scores)
+from gpu_common import (GpuRun, assert_out_close, assert_scores_equal, check_topk_definition,
+                        need_gpu, oracle_attn, oracle_scores)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _full_check(case, ld=None):
     g = GpuRun(case, ld=ld)
     s = g.scores().cpu().numpy()
     s_ref = oracle_scores(case, ld=s.shape[1])
-    np.testing.assert_array_equal(s, s_ref)
+    assert_scores_equal(s, s_ref, case.n_elig)
     idx = g.topk().cpu().numpy()
     idx_ref = oracle.topk(s_ref, case.n_elig, case.K)
     np.testing.assert_array_equal(idx, idx_ref)
@@ -67,7 +67,7 @@ def test_prefill_sampled_rows_k2048():
     out, lse = g.all()
     rows = np.array([0, 1, 63, 64, 1000, 2046, 2047, 2048, 2049, 2500, 2599])
     s_ref = oracle_scores(c, rows=rows)
-    np.testing.assert_array_equal(g.pipe.scores.cpu().numpy()[rows], s_ref)
+    assert_scores_equal(g.pipe.scores.cpu().numpy()[rows], s_ref, c.n_elig[rows])
     idx_ref = oracle.topk(s_ref, c.n_elig[rows], c.K)
     np.testing.assert_array_equal(g.pipe.idx.cpu().numpy()[rows], idx_ref)
     out_ref, lse_ref = oracle_attn(c, idx_ref, rows=rows)
@@ -176,3 +176,32 @@ def test_bad_block_id_is_flagged_not_faulted():
     c.block_table[0, 3] = 0                          # oracle needs a valid table for row 0
     out_ref, lse_ref = oracle_attn(c, ok)
     assert_out_close(out[1:], lse[1:], out_ref[1:], lse_ref[1:], "skipped row")
+
+
+def test_fp8_indexer_adversarial_exactness():
+    """Integer dot products up to +-8192 per head (14 significant bits) with
+    mixtures of large and small products: the FP8 tensor-core accumulation must
+    keep every bit, so scores stay bit-exact."""
+    need_gpu()
+    c = W.make_case("fp8-adv", seed=900, seq_lens=(1100, 700, 257), K=128, **LAT_SHAPES)
+    rng = np.random.default_rng(2)
+    D = c.D_i
+    pats = [np.full(D, 8), np.full(D, -8), np.r_[np.full(64, 8), np.full(64, 1)],
+            np.r_[np.full(64, 8), np.full(64, -8)], np.r_[np.full(127, 8), [1]],
+            np.tile([8, 1], D // 2), np.tile([8, -8, 1, 1], D // 4), np.full(D, 1)]
+    q = np.empty((c.Nq, c.H_i, D), np.int64)
+    for r in range(c.Nq):
+        for h in range(c.H_i):
+            q[r, h] = pats[(r + h) % len(pats)] * (1 if h % 3 else -1)
+    k = np.empty(c.kidx_pool.shape, np.int64)
+    flat = k.reshape(-1, D)
+    for i in range(flat.shape[0]):
+        flat[i] = pats[rng.integers(len(pats))] if i % 5 else rng.integers(-8, 9, D)
+    c.q_idx = W.encode_int(q, "fp8")
+    c.kidx_pool = W.encode_int(k, "fp8")
+    c.w[:] = 4.0
+    g = GpuRun(c)
+    s = g.scores().cpu().numpy()
+    s_ref = oracle_scores(c, ld=s.shape[1])
+    assert s_ref[np.isfinite(s_ref)].max() >= 8192 * 4
+    assert_scores_equal(s, s_ref, c.n_elig)
