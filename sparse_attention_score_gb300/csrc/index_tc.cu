@@ -291,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
         const int acc = it & 1;
-        if (!mbar_wait(&s.accfull[acc], (it >> 1) & 1, &s.abort)) {
+        // warp-uniform outcome: the TMEM loads below are .sync.aligned
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&s.accfull[acc], (it >> 1) & 1, &s.abort));
+        if (!ok) {
           fail(s, a.status);
           break;
         }
