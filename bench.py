@@ -190,7 +190,8 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
                                    pipe.out, pipe.lse, pipe.ws_attn)
         else:
             dsa.sparse_attn_prefill(layout, d.q, d.k_pool, d.v_pool, pipe.idx, case.sm_scale,
-                                    pipe.out, pipe.lse, pipe.ws_attn, q_seq=d.q_seq)
+                                    pipe.out, pipe.lse, pipe.ws_attn, q_seq=d.q_seq,
+                                    q_pos=d.q_pos)
         if evs:
             evs[3].record(stream)
 

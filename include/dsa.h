@@ -181,6 +181,10 @@ int dsa_sparse_attn_decode(const dsa_paged_layout* layout, const void* q, const 
  * sequence q_seq[r]:
  *  q            [Nq][Hq][Dqk] bf16
  *  q_seq        [Nq] int32 sequence of each query, or NULL: all in sequence 0
+ *  q_pos        [Nq] int32 absolute position of each query, or NULL.  When
+ *               given, only the first min(K, q_pos+1) entries of idx[r] are
+ *               read and an index > q_pos (non-causal) is skipped and flagged
+ *               DSA_STATUS_BAD_INDEX
  *  idx          [Nq][K] int32
  *  out          [Nq][Hq][Dv] bf16, lse [Nq][Hq] fp32 or NULL
  *  ws           workspace of dsa_sparse_attn_prefill_workspace_size() bytes
@@ -189,9 +193,10 @@ int dsa_sparse_attn_decode(const dsa_paged_layout* layout, const void* q, const 
 size_t dsa_sparse_attn_prefill_workspace_size(int Nq, int Hq, int Dqk, int Dv, int K);
 int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const void* k_pool,
                             int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
-                            int Hq, int Dqk, int Dv, const int32_t* q_seq, int Nq,
-                            const int32_t* idx, int K, float sm_scale, void* out, float* lse,
-                            void* ws, size_t ws_bytes, dsa_stream_t stream);
+                            int Hq, int Dqk, int Dv, const int32_t* q_seq,
+                            const int32_t* q_pos, int Nq, const int32_t* idx, int K,
+                            float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                            dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Utilities (no counterpart on the pages).

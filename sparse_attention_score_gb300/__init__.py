@@ -85,8 +85,8 @@ _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
 _sig("dsa_sparse_attn_decode", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _f, _vp,
                                     _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_prefill_workspace_size", _sz, [_i, _i, _i, _i, _i])
-_sig("dsa_sparse_attn_prefill", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _vp, _i,
-                                     _f, _vp, _vp, _vp, _sz, _vp])
+_sig("dsa_sparse_attn_prefill", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _vp, _i, _vp,
+                                     _i, _f, _vp, _vp, _vp, _sz, _vp])
 
 SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_status",
            "dsa_index_score_workspace_size", "dsa_index_score", "dsa_topk_workspace_size",
@@ -206,13 +206,13 @@ def sparse_attn_decode(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, ou
 
 
 def sparse_attn_prefill(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
-                        q_seq=None, stream=None):
+                        q_seq=None, q_pos=None, stream=None):
     Nq, Hq, Dqk = q.shape
     Dv = out.shape[2]
     rc = _lib.dsa_sparse_attn_prefill(layout.c(), _ptr(q), _ptr(k_pool), k_pool.shape[-1],
-                                      _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(q_seq), Nq,
-                                      _ptr(idx), idx.shape[1], float(sm_scale), _ptr(out),
-                                      _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+                                      _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(q_seq),
+                                      _ptr(q_pos), Nq, _ptr(idx), idx.shape[1], float(sm_scale),
+                                      _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "dsa_sparse_attn_prefill")
 
 
@@ -262,7 +262,7 @@ class Pipeline:
                                self.lse, self.ws_attn, stream=stream)
         else:
             sparse_attn_prefill(self.layout, q, k_pool, v_pool, self.idx, sm_scale, self.out,
-                                self.lse, self.ws_attn, q_seq=q_seq, stream=stream)
+                                self.lse, self.ws_attn, q_seq=q_seq, q_pos=q_pos, stream=stream)
         return self.out
 
     def status(self) -> int:

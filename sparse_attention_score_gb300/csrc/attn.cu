@@ -11,7 +11,8 @@
 // unnormalised partial (o, m, l) and a combine kernel merges them:
 //     M = max_s m_s,  l = sum_s l_s 2^(m_s - M),  o = sum_s o_s 2^(m_s - M) / l.
 //
-// This file holds the CUDA-core kernel used for every supported shape.
+// This file holds the CUDA-core kernel, used for every shape the tensor-core
+// kernel (attn_tc.cu) does not cover.
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
 
@@ -52,7 +53,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
 
   const int per = (a.K + S - 1) / S;
   const int j0 = split * per, j1 = min(a.K, j0 + per);
-  const long long L = b_ok ? (long long)__ldg(&a.lay.seq_lens[b]) : 0;
+  long long L = b_ok ? (long long)__ldg(&a.lay.seq_lens[b]) : 0;
+  if (a.q_pos) {
+    const long long qp = (long long)__ldg(&a.q_pos[r]) + 1;  // positions <= q_pos
+    if (qp < L) L = qp;
+  }
   for (int j = j0; j < j1; ++j) {
     if (threadIdx.x == 0) {
       long long row = -1;
@@ -212,14 +217,18 @@ bool attn_supported(int Hq, int Dqk, int Dv) {
          Dv <= 512 && (size_t)Hq * Dqk * 2 + 4 * (Dqk + Dv) <= 200 * 1024;
 }
 
-size_t attn_ws(int Nq, int Hq, int, int Dv, int K, bool) {
+size_t attn_ws(int Nq, int Hq, int Dqk, int Dv, int K, bool) {
   const int S = choose_splits(Nq, K);
-  if (S == 1) return kWsHeader;
-  return kWsHeader + sizeof(float) * (size_t)Nq * S * Hq * ((size_t)Dv + 2);
+  size_t generic = kWsHeader;
+  if (S > 1) generic += sizeof(float) * (size_t)Nq * S * Hq * ((size_t)Dv + 2);
+  size_t tc = 0;
+  if (Hq == 64 && Dqk == 576 && Dv == 512) tc = attn_tc_ws(Nq);
+  return generic > tc ? generic : tc;
 }
 
-int launch_attn(AttnParams p, bool /*decode*/, void* ws, size_t /*ws_bytes*/, cudaStream_t s) {
+int launch_attn(AttnParams p, bool /*decode*/, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (p.Nq == 0) return DSA_OK;
+  if (attn_tc_eligible(p) && ws_bytes >= attn_tc_ws(p.Nq)) return launch_attn_tc(p, ws, s);
   p.S = choose_splits(p.Nq, p.K);
   if (p.S > 1) {
     p.part_o = reinterpret_cast<float*>((char*)ws + kWsHeader);

@@ -148,7 +148,8 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
 
 static int attn_common(const dsa_paged_layout* layout, const void* q, const void* k_pool,
                        int64_t k_row_stride, const void* v_pool, int64_t v_row_stride, int Hq,
-                       int Dqk, int Dv, const int32_t* q_seq, int Nq, const int32_t* idx, int K,
+                       int Dqk, int Dv, const int32_t* q_seq, const int32_t* q_pos, int Nq,
+                       const int32_t* idx, int K,
                        float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
                        dsa_stream_t stream, bool decode) {
   AttnParams p{};
@@ -179,6 +180,7 @@ static int attn_common(const dsa_paged_layout* layout, const void* q, const void
   p.Dqk = Dqk;
   p.Dv = Dv;
   p.q_seq = q_seq;
+  p.q_pos = q_pos;
   p.seq0 = decode ? 0 : 1;
   p.Nq = Nq;
   p.idx = idx;
@@ -201,7 +203,7 @@ int dsa_sparse_attn_decode(const dsa_paged_layout* layout, const void* q, const 
                            dsa_stream_t stream) {
   int B = layout ? layout->batch : 0;
   return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, nullptr,
-                     B, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, true);
+                     nullptr, B, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, true);
 }
 
 size_t dsa_sparse_attn_prefill_workspace_size(int Nq, int Hq, int Dqk, int Dv, int K) {
@@ -210,11 +212,12 @@ size_t dsa_sparse_attn_prefill_workspace_size(int Nq, int Hq, int Dqk, int Dv, i
 
 int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const void* k_pool,
                             int64_t k_row_stride, const void* v_pool, int64_t v_row_stride,
-                            int Hq, int Dqk, int Dv, const int32_t* q_seq, int Nq,
-                            const int32_t* idx, int K, float sm_scale, void* out, float* lse,
-                            void* ws, size_t ws_bytes, dsa_stream_t stream) {
+                            int Hq, int Dqk, int Dv, const int32_t* q_seq,
+                            const int32_t* q_pos, int Nq, const int32_t* idx, int K,
+                            float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                            dsa_stream_t stream) {
   return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, q_seq,
-                     Nq, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, false);
+                     q_pos, Nq, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, false);
 }
 
 }  // extern "C"

@@ -57,6 +57,7 @@ struct AttnParams {
   int Hq, Dqk, Dv;
   const int32_t* q_seq;  // NULL: query r is sequence r (decode) / sequence 0 (prefill)
   int seq0;              // 1: q_seq NULL means every query is in sequence 0
+  const int32_t* q_pos;  // NULL or [Nq]: causal bound of each query (prefill)
   int Nq;
   const int32_t* idx;
   int K;
@@ -93,6 +94,10 @@ int launch_topk(const TopkParams& p, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t topk_ws(int Nq, long long ld, int K);
 
 int launch_attn(AttnParams p, bool decode, void* ws, size_t ws_bytes, cudaStream_t s);
+// tensor-core attention (64 heads, latent 576/512 rows shared by K and V)
+bool attn_tc_eligible(const AttnParams& p);
+size_t attn_tc_ws(int Nq);
+int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s);
 bool attn_supported(int Hq, int Dqk, int Dv);
 size_t attn_ws(int Nq, int Hq, int Dqk, int Dv, int K, bool decode);
 

@@ -79,7 +79,8 @@ class GpuRun:
                                         p.lse, p.ws_attn)
         else:
             self.dsa.sparse_attn_prefill(self.layout, d.q, d.k_pool, d.v_pool, ix, c.sm_scale,
-                                         p.out, p.lse, p.ws_attn, q_seq=d.q_seq)
+                                         p.out, p.lse, p.ws_attn, q_seq=d.q_seq,
+                                         q_pos=d.q_pos)
         return p.out, p.lse
 
     def all(self):

@@ -114,7 +114,7 @@ def test_attention_rejects_bad_arguments(dsa):
     assert dec(ws=None) == -3
     okp = dsa.sparse_attn_prefill_workspace_size(3, 16, 128, 128, 64)
     assert lib.dsa_sparse_attn_prefill(ctypes.byref(lay), FAKE, FAKE, 128, FAKE, 128, 16, 128,
-                                       128, None, 3, FAKE, 0, 0.1, FAKE, None, FAKE, okp,
+                                       128, None, None, 3, FAKE, 0, 0.1, FAKE, None, FAKE, okp,
                                        None) == -1
 
 

@@ -205,3 +205,36 @@ def test_fp8_indexer_adversarial_exactness():
     s_ref = oracle_scores(c, ld=s.shape[1])
     assert s_ref[np.isfinite(s_ref)].max() >= 8192 * 4
     assert_scores_equal(s, s_ref, c.n_elig)
+
+
+def test_attention_running_max_rescale_path():
+    """Scores that jump by far more than 2^8 from one 128-row tile to the next
+    (for even heads only) force the O rescale in the online softmax."""
+    need_gpu()
+    c = W.make_case("rescale", seed=950, seq_lens=(700, 1500), K=512, **LAT_SHAPES)
+    kp = c.k_pool.astype(np.uint16).copy()
+    lvl = [0.0, 0.25, 0.5, 1.0]
+    for b in range(c.B):
+        L = int(c.seq_lens[b])
+        for p in range(L):
+            page, slot = c.block_table[b, p // c.bs], p % c.bs
+            val = lvl[min(p // 128, 3)]
+            row = np.full(c.Dqk, val, np.float32)
+            row[c.Dv:] = val
+            # keep V informative: first dims carry the position
+            row[0] = (p % 97) / 97.0
+            kp[page, slot] = W.encode_bf16(row)
+    c.k_pool = c.v_pool = kp
+    qf = np.ones((c.Nq, c.Hq, c.Dqk), np.float32)
+    qf[:, 1::2, :] = -1.0
+    qf[:, :, 0] = 0.0
+    c.q = W.encode_bf16(qf)
+    g = GpuRun(c)
+    idx = np.full((c.B, c.K), -1, np.int32)
+    for b in range(c.B):
+        n = min(c.K, int(c.seq_lens[b]))
+        idx[b, :n] = np.arange(n)
+    out, lse = g.attn(torch.from_numpy(idx).cuda())
+    out_ref, lse_ref = oracle_attn(c, idx)
+    assert_out_close(out, lse, out_ref, lse_ref, "rescale")
+    assert g.status() == 0
