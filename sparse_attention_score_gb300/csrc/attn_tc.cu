@@ -18,20 +18,23 @@
 //   PV  O^T[512 dv x 64 heads] += V^T[512 x 128 rows] . P^T[128 rows x 64]
 //       A = V^T (the first 512 dims of the same rows, MN-major), B = P^T
 //       (MN-major, one 128-byte row per KV row); 4 blocks of 128 dv.
+// P is rounded to bf16 as hi + lo (two PV MMAs) and the softmax denominators
+// sum exactly the values the MMA multiplies, so the only rounding left in the
+// output is the final bf16 store.
 // The tiles of all queries are laid end to end and split evenly over one CTA
 // per SM.  A query whose tiles span several CTAs leaves one unnormalised
-// partial (O, m, l) per CTA in the workspace; the CTA that finishes last
-// (atomic counter, no waiting) merges them:
-//   M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
+// partial (O, m, l) per CTA in the workspace and a second small kernel merges
+// them:  M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
 //
-// Warp roles (320 threads):
-//   warps 0-3 softmax; warps 4-7 epilogue (O out of TMEM, partials, merge);
-//   warp 8 producer (TMA: Q, then per tile 9 K chunks and, one tile later, the
-//   8 V chunks again, rows gathered four at a time with tile::gather4);
-//   warp 9 TMEM owner and MMA issuer.  QK of tile i is issued before PV of
+// Warp roles (288 threads):
+//   warps 0-3 softmax, and at the end of each query segment O out of TMEM;
+//   warps 4-7 producer: Q by TMA; per tile the 9 K chunks and, one tile
+//   later, the 8 V chunks again, one row per thread, 16-byte cp.async into
+//   the 128-byte swizzled layout (rows of 1152 bytes anywhere in the pool);
+//   warp 8 TMEM owner and MMA issuer.  QK of tile i is issued before PV of
 //   tile i-1, so the softmax of one tile overlaps the MMAs of the next.
 // Selected rows that are padding, past the sequence, non-causal or behind a
-// bad block id are read as zeros (out-of-range TMA rows) and masked to -inf.
+// bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
@@ -51,7 +54,7 @@ constexpr int kRing = 3;                     // pair slots
 constexpr int kQChunks = kDqk / 64;          // 9
 constexpr int kQChunkBytes = kHq * 128;      // 8 KB
 constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
-constexpr int kThreads = 320;
+constexpr int kThreads = 288;                // 4 softmax + 4 producer + 1 MMA warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
 constexpr uint32_t kColO = 128;  // four 64-column O^T blocks
@@ -63,16 +66,15 @@ constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
 struct __align__(1024) Smem {
   uint8_t q[kQChunks][kQChunkBytes];
   uint8_t ring[kRing][kPairBytes];
-  uint8_t pt[2][kPBytes];
-  uint64_t qfull, qempty, full[kRing], empty[kRing], sfull[2], sempty[2], pfull[2], pempty[2];
-  uint64_t pvdone, ofull, ofree, statfull, statempty, done, smsync, epsync;
+  uint8_t phi[kPBytes];  // P^T, bf16 part
+  uint8_t plo[kPBytes];  // P^T, bf16 remainder (P - phi)
+  uint64_t qfull, qempty, full[kRing], empty[kRing], sfull[2], sempty[2], pfull, pempty;
+  uint64_t ofull, ofree, smsync, done;
   uint32_t tmem_base;
   int abort;
   int rescale[2];
-  int combine;
   float redm[4][kHq], reds[4][kHq];
   float m_used[kHq], fscale[kHq], l_run[kHq];
-  float stat_m[kHq], stat_l[kHq];
 };
 
 struct Geo {
@@ -80,8 +82,8 @@ struct Geo {
   long long total;
   int G;
   long long lo, hi;
-  __device__ long long lo_of(int c) const { return (long long)c * total / G; }
-  __device__ int cta_of(long long x) const {
+  __host__ __device__ long long lo_of(int c) const { return (long long)c * total / G; }
+  __host__ __device__ int cta_of(long long x) const {
     int c = (int)(x * G / total);
     while (c + 1 < G && lo_of(c + 1) <= x) ++c;
     while (c > 0 && lo_of(c) > x) --c;
@@ -132,11 +134,14 @@ __device__ __forceinline__ Seg make_seg(const AttnParams& a, const Geo& g, int r
   return s;
 }
 
-// Physical row of selected entry j of a query, or -1 if it is not usable.
-__device__ __forceinline__ long long sel_row(const AttnParams& a, const Seg& s, long long j,
-                                             bool flag) {
+// Selected position of entry j of a query (-1: none / padding).
+__device__ __forceinline__ int sel_pos(const AttnParams& a, const Seg& s, long long j) {
   if (j >= s.n || s.b < 0) return -1;
-  const int p = __ldg(&a.idx[(long long)s.r * a.K + j]);
+  return __ldg(&a.idx[(long long)s.r * a.K + j]);
+}
+
+// Physical row of a selected position, or -1 if it is not usable.
+__device__ __forceinline__ long long pos_row(const AttnParams& a, const Seg& s, int p, bool flag) {
   if (p < 0) return -1;
   if (p >= s.L || (s.qp >= 0 && p > s.qp)) {
     if (flag) flag_status(a.status, DSA_STATUS_BAD_INDEX);
@@ -146,6 +151,34 @@ __device__ __forceinline__ long long sel_row(const AttnParams& a, const Seg& s, 
   if (row < 0 && flag) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
   return row;
 }
+
+// Active tiles of this CTA in order (segments without active tiles skipped).
+struct Walker {
+  int r, r_last, t;
+  Seg s;
+  bool ok;
+  __device__ void settle(const AttnParams& a, const Geo& g) {
+    while (ok && t >= s.act_end) {
+      if (++r > r_last) { ok = false; break; }
+      s = make_seg(a, g, r);
+      t = s.t0;
+    }
+  }
+  __device__ void init(const AttnParams& a, const Geo& g, int r0, int r1) {
+    r = r0;
+    r_last = r1;
+    ok = r0 <= r1;
+    if (ok) {
+      s = make_seg(a, g, r);
+      t = s.t0;
+      settle(a, g);
+    }
+  }
+  __device__ void next(const AttnParams& a, const Geo& g) {
+    ++t;
+    settle(a, g);
+  }
+};
 
 __device__ __forceinline__ void fail(Smem& sm, int* status) {
   sm.abort = 1;
@@ -177,11 +210,6 @@ __device__ __forceinline__ int butterfly_head(int lane) {
          4 * ((lane >> 1) & 1) + 2 * (lane & 1);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
@@ -196,9 +224,21 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volat
   return ok;
 }
 
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    k_attn_tc(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
-              AttnParams a, float* part_o, float* part_ml, int* counters) {
+    k_attn_tc(const __grid_constant__ CUtensorMap map_q, AttnParams a, float* part_o,
+              float* part_ml) {
   extern __shared__ uint8_t smraw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   g.hi = g.lo_of(blockIdx.x + 1);
   const int r_first = (int)(g.lo / g.Tq);
   const int r_last = g.hi > g.lo ? (int)((g.hi - 1) / g.Tq) : r_first - 1;
-  const int oob_row = a.lay.nb * a.lay.bs;  // read as zeros by TMA
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -219,112 +258,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.qfull, 1);
     mbar_init(&sm.qempty, 1);
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.full[i], 128);
       mbar_init(&sm.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.sfull[i], 1);
       mbar_init(&sm.sempty[i], 128);
-      mbar_init(&sm.pfull[i], 128);
-      mbar_init(&sm.pempty[i], 1);
     }
-    mbar_init(&sm.pvdone, 1);
+    mbar_init(&sm.pfull, 128);
+    mbar_init(&sm.pempty, 1);
     mbar_init(&sm.ofull, 1);
     mbar_init(&sm.ofree, 128);
-    mbar_init(&sm.statfull, 32);
-    mbar_init(&sm.statempty, 128);
-    mbar_init(&sm.done, 1);
     mbar_init(&sm.smsync, 128);
-    mbar_init(&sm.epsync, 128);
+    mbar_init(&sm.done, 1);
     fence_mbar_init();
   }
   if (threadIdx.x < kHq) {
     sm.m_used[threadIdx.x] = -INFINITY;
     sm.l_run[threadIdx.x] = 0.0f;
   }
-  if (warp == 9) {
+  if (warp == 8) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&map_kv);
-    tma_prefetch_desc(&map_q);
-  }
+  if (warp == 4 && lane == 0) tma_prefetch_desc(&map_q);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
 
-  if (warp == 8) {
+  if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ producer --
-    int slot = 0;
-    uint32_t phase = 0;
-    int issued = 0, sa = 0;
-    uint32_t issued_parity[kRing];
-    int rk[4], rv[4];
-    bool have_prev = false, ok = true;
-    auto load_pairs = [&](int first_chunk, int nchunks, const int (&rows)[4]) -> bool {
-      for (int c = first_chunk; c < first_chunk + nchunks; c += 2) {
-        const int nc = min(2, first_chunk + nchunks - c);
-        bool w = true;
-        if (lane == 0) {
-          w = mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort);
-          if (w) mbar_arrive_expect_tx(&sm.full[slot], nc * kChunkBytes);
-        }
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) return false;
-        for (int i = 0; i < nc; ++i)
-          tma_gather4(sm.ring[slot] + i * kChunkBytes + lane * 512, &map_kv, &sm.full[slot],
-                      64 * (c + i), rows[0], rows[1], rows[2], rows[3]);
-        issued_parity[slot] = phase;
-        ++issued;
-        if (++slot == kRing) {
-          slot = 0;
-          phase ^= 1;
-        }
+    // Thread `row` copies row `row` of every chunk of every tile: 8 x 16 B per
+    // 64-dim chunk, placed in the 128-byte swizzled K-major layout.
+    const int row = threadIdx.x - 128;
+    const char* kv = reinterpret_cast<const char*>(a.kp);
+    int j = 0;            // pairs issued
+    int signalled = 0;    // pairs signalled full
+    int sa = 0;
+    bool ok = true;
+    auto signal_one = [&]() {
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.full[signalled % kRing]);
+      ++signalled;
+    };
+    auto flush = [&]() {
+      cp_async_wait<0>();
+      while (signalled < j) signal_one();
+    };
+    auto issue_pair = [&](int c0, int nc, long long prow) -> bool {
+      const int slot = j % kRing;
+      const uint32_t par = ((j / kRing) & 1) ^ 1;
+      if (!warp_wait(&sm.empty[slot], par, &sm.abort)) return false;
+      const uint32_t nbytes = prow >= 0 ? 16u : 0u;
+      const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) : kv;
+      uint8_t* dst = sm.ring[slot] + row * 128;
+      for (int i = 0; i < nc; ++i) {
+#pragma unroll
+        for (int gq = 0; gq < 8; ++gq)
+          cp_async16(dst + i * kChunkBytes + ((gq ^ (row & 7)) << 4),
+                     src + (c0 + i) * 128 + (prow >= 0 ? gq * 16 : 0), nbytes);
+      }
+      cp_async_commit();
+      ++j;
+      if (j - signalled > 2) {
+        cp_async_wait<2>();
+        signal_one();
       }
       return true;
     };
-    for (int r = r_first; r <= r_last && ok; ++r) {
-      const Seg s = make_seg(a, g, r);
-      if (s.active() == 0) continue;
-      bool w = true;
-      if (lane == 0) {
-        if (sa > 0) w = mbar_wait(&sm.qempty, (sa - 1) & 1, &sm.abort);
-        if (w) {
-          mbar_arrive_expect_tx(&sm.qfull, kQChunks * kQChunkBytes);
-          for (int c = 0; c < kQChunks; ++c)
-            tma_load_2d(sm.q[c], &map_q, &sm.qfull, 64 * c, r * kHq);
+    Walker w;
+    w.init(a, g, r_first, r_last);
+    int cur_r = -1;
+    long long prev_row = -1;
+    bool have_prev = false;
+    int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + row) : -1;
+    while (w.ok && ok) {
+      if (w.r != cur_r) {
+        // new query: drain, wait for the previous Q to be consumed, load Q
+        flush();
+        bool qok = true;
+        if (threadIdx.x == 128) {
+          if (sa > 0) qok = mbar_wait(&sm.qempty, (sa - 1) & 1, &sm.abort);
+          if (qok) {
+            mbar_arrive_expect_tx(&sm.qfull, kQChunks * kQChunkBytes);
+            for (int c = 0; c < kQChunks; ++c)
+              tma_load_2d(sm.q[c], &map_q, &sm.qfull, 64 * c, w.r * kHq);
+          }
         }
+        if (!__shfl_sync(0xffffffffu, qok, 0) && warp == 4) { ok = false; break; }
+        cur_r = w.r;
+        ++sa;
       }
-      if (!__shfl_sync(0xffffffffu, w, 0)) {
-        ok = false;
-        break;
-      }
-      for (int t = s.t0; t < s.act_end; ++t) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const long long row = sel_row(a, s, (long long)t * kRows + lane * 4 + e, false);
-          rk[e] = row < 0 ? oob_row : (int)row;
-        }
-        if (!load_pairs(0, kQChunks, rk)) { ok = false; break; }
-        if (have_prev && !load_pairs(0, kDv / 64, rv)) { ok = false; break; }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) rv[e] = rk[e];
-        have_prev = true;
-      }
-      ++sa;
+      const long long row_cur = pos_row(a, w.s, p_cur, false);
+      // look one tile ahead for the position this thread copies next
+      Walker nx = w;
+      nx.next(a, g);
+      const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + row) : -1;
+      for (int c = 0; c < kQChunks && ok; c += 2) ok = issue_pair(c, min(2, kQChunks - c), row_cur);
+      if (ok && have_prev)
+        for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, prev_row);
+      prev_row = row_cur;
+      have_prev = true;
+      p_cur = p_next;
+      w = nx;
     }
-    if (ok && have_prev) ok = load_pairs(0, kDv / 64, rv);
-    if (!ok && lane == 0) fail(sm, a.status);
-    if (lane == 0) {
-      const int pend = issued < kRing ? issued : kRing;
-      for (int i = 0; i < pend; ++i) {
-        const int st = (slot - 1 - i + 2 * kRing) % kRing;
-        mbar_wait(&sm.full[st], issued_parity[st], &sm.abort, 100000000ull);
-      }
-    }
-  } else if (warp == 9) {
+    if (ok && have_prev)
+      for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, prev_row);
+    flush();
+    if (!ok) fail(sm, a.status);
+  } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       int slot = 0;
@@ -346,67 +389,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto do_pv = [&](const Prev& p) -> bool {
-        if (!mbar_wait(&sm.pfull[p.u & 1], (p.u >> 1) & 1, &sm.abort)) return false;
+        if (!mbar_wait(&sm.pfull, p.u & 1, &sm.abort)) return false;
         if (p.first && p.seg > 0 && !mbar_wait(&sm.ofree, (p.seg - 1) & 1, &sm.abort)) return false;
         tc_fence_after();
-        const uint32_t pt0 = smem_u32(sm.pt[p.u & 1]);
+        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
         for (int blk = 0; blk < kDv / 128; ++blk) {
           if (!consume()) return false;
           const uint32_t v0 = smem_u32(sm.ring[slot]);
+          const uint32_t d = tbase + kColO + 64 * blk;
 #pragma unroll
           for (int k = 0; k < kRows / 16; ++k) {
-            mma_f16(tbase + kColO + 64 * blk, smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B),
-                    smem_desc(pt0 + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+            const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
+            mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
                     (p.first && k == 0) ? 0u : 1u);
+            mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
           }
           release();
         }
-        mma_commit(&sm.pempty[p.u & 1]);
-        mma_commit(&sm.pvdone);
+        mma_commit(&sm.pempty);
         if (p.last) mma_commit(&sm.ofull);
         return true;
       };
-      for (int r = r_first; r <= r_last && ok; ++r) {
-        const Seg s = make_seg(a, g, r);
-        if (s.active() == 0) continue;
-        if (!mbar_wait(&sm.qfull, sa & 1, &sm.abort)) { ok = false; break; }
+      Walker w;
+      w.init(a, g, r_first, r_last);
+      int cur_r = -1;
+      while (w.ok && ok) {
+        if (w.r != cur_r) {
+          if (!mbar_wait(&sm.qfull, sa & 1, &sm.abort)) { ok = false; break; }
+          cur_r = w.r;
+          ++sa;
+        }
+        if (!mbar_wait(&sm.sempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t q0 = smem_u32(sm.q[0]);
-        for (int t = s.t0; t < s.act_end; ++t) {
-          if (!mbar_wait(&sm.sempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t dS = tbase + kColS + 64 * (u & 1);
-          for (int c = 0; c < kQChunks && ok; c += 2) {
-            if (!consume()) { ok = false; break; }
-            const uint32_t a0 = smem_u32(sm.ring[slot]);
-            for (int i = 0; i < 2 && c + i < kQChunks; ++i) {
+        const uint32_t dS = tbase + kColS + 64 * (u & 1);
+        for (int c = 0; c < kQChunks && ok; c += 2) {
+          if (!consume()) { ok = false; break; }
+          const uint32_t a0 = smem_u32(sm.ring[slot]);
+          for (int i = 0; i < 2 && c + i < kQChunks; ++i) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                mma_f16(dS, smem_desc(a0 + i * kChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
-                        smem_desc(q0 + (c + i) * kQChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
-                        kIdescQK, (c + i + k) > 0 ? 1u : 0u);
-              }
+            for (int k = 0; k < 4; ++k) {
+              mma_f16(dS, smem_desc(a0 + i * kChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
+                      smem_desc(q0 + (c + i) * kQChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
+                      kIdescQK, (c + i + k) > 0 ? 1u : 0u);
             }
-            release();
           }
-          if (!ok) break;
-          mma_commit(&sm.sfull[u & 1]);
-          if (t == s.act_end - 1) mma_commit(&sm.qempty);
-          if (have_prev && !do_pv(prev)) { ok = false; break; }
-          prev = Prev{u, sa, t == s.t0, t == s.act_end - 1};
-          have_prev = true;
-          ++u;
+          release();
         }
-        ++sa;
+        if (!ok) break;
+        mma_commit(&sm.sfull[u & 1]);
+        const bool first = (w.t == w.s.t0), last = (w.t == w.s.act_end - 1);
+        if (last) mma_commit(&sm.qempty);
+        if (have_prev && !do_pv(prev)) { ok = false; break; }
+        prev = Prev{u, sa - 1, first, last};
+        have_prev = true;
+        ++u;
+        w.next(a, g);
       }
       if (ok && have_prev) ok = do_pv(prev);
       if (!ok) fail(sm, a.status);
       mma_commit(&sm.done);
       mbar_wait(&sm.done, 0, &sm.abort, 100000000ull);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------- softmax --
-    const int row = threadIdx.x;  // TMEM lane = row of the tile
+  } else {
+    // ------------------------------------------------- softmax + finalize --
+    const int row = threadIdx.x;  // TMEM lane = row of the tile = dv lane of O
     const int hb = butterfly_head(lane);
     const float c = a.scale_log2;
     int u = 0, sa = 0;
@@ -414,9 +461,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int r = r_first; r <= r_last && ok; ++r) {
       const Seg s = make_seg(a, g, r);
-      if (s.active() == 0) continue;
+      const int pslot = 2 * blockIdx.x + (((long long)r * g.Tq > g.lo) ? 1 : 0);
+      float* po = part_o + (size_t)pslot * kHq * kDv;
+      float* pml = part_ml + (size_t)pslot * kHq * 2;
+      __nv_bfloat16* out = a.out + (size_t)r * kHq * kDv;
+      if (s.active() == 0) {
+        if (s.complete) {
+          for (int i = row; i < kHq * kDv; i += 128) out[i] = __float2bfloat16(0.0f);
+          if (a.lse && row < kHq) a.lse[(size_t)r * kHq + row] = -INFINITY;
+        } else if (row < kHq) {
+          pml[2 * row] = -INFINITY;
+          pml[2 * row + 1] = 0.0f;
+        }
+        continue;
+      }
       for (int t = s.t0; t < s.act_end; ++t) {
-        const bool valid = sel_row(a, s, (long long)t * kRows + row, true) >= 0;
+        const bool valid =
+            pos_row(a, s, sel_pos(a, s, (long long)t * kRows + row), true) >= 0;
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         float z[kHq], v[kHq];
@@ -463,15 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
         const bool resc = sm.rescale[u & 1] != 0;
         if (threadIdx.x == 0) sm.rescale[(u + 1) & 1] = 0;
+        // P = 2^(z - m), kept as the exact fp32 sum of its bf16 hi and lo parts
+        // (the values the two PV MMAs multiply); the row sums use the same.
 #pragma unroll
         for (int h = 0; h < kHq; ++h) {
           const float mu = sm.m_used[h];
-          z[h] = (mu == -INFINITY) ? 0.0f : exp2f(z[h] - mu);
+          const float pf = (mu == -INFINITY) ? 0.0f : exp2f(z[h] - mu);
+          const float hi = __bfloat162float(__float2bfloat16_rn(pf));
+          z[h] = hi + __bfloat162float(__float2bfloat16_rn(pf - hi));
         }
+        // the previous PV must be done before P^T (and, if needed, O) change
+        if (!warp_wait(&sm.pempty, (u & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        tc_fence_after();
         if (resc) {
-          // O (tiles before this one) must be complete before it is rescaled
-          if (!warp_wait(&sm.pvdone, (u - 1) & 1, &sm.abort)) { ok = false; break; }
-          tc_fence_after();
           for (int blk = 0; blk < kDv / 128; ++blk) {
             for (int half = 0; half < 2; ++half) {
               uint32_t raw[32];
@@ -485,32 +550,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tmem_wait_st();
-          tc_fence_before();
         }
-        // P^T row: 64 heads as bf16, 128-byte row, 16-byte granules swizzled
-        if (!warp_wait(&sm.pempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         {
-          uint8_t* prow = sm.pt[u & 1] + row * 128;
+          uint8_t* rh = sm.phi + row * 128;
+          uint8_t* rl = sm.plo + row * 128;
 #pragma unroll
           for (int gq = 0; gq < 8; ++gq) {
-            uint4 pk;
-            pk.x = pack_bf16(z[8 * gq + 0], z[8 * gq + 1]);
-            pk.y = pack_bf16(z[8 * gq + 2], z[8 * gq + 3]);
-            pk.z = pack_bf16(z[8 * gq + 4], z[8 * gq + 5]);
-            pk.w = pack_bf16(z[8 * gq + 6], z[8 * gq + 7]);
-            *reinterpret_cast<uint4*>(prow + ((gq ^ (row & 7)) << 4)) = pk;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a0 = z[8 * gq + 2 * k], a1 = z[8 * gq + 2 * k + 1];
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
+              const float2 hf = __bfloat1622float2(hi);
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+              hw[k] = *reinterpret_cast<const uint32_t*>(&hi);
+              lw[k] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+            const int off = (gq ^ (row & 7)) << 4;
+            *reinterpret_cast<uint4*>(rh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(rl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&sm.pfull[u & 1]);
-        // per-head tile sum (of the fp32 probabilities)
+        tc_fence_before();
+        mbar_arrive(&sm.pfull);
+        // per-head tile sum of the probabilities as the MMA sees them
 #pragma unroll
         for (int h = 0; h < kHq; ++h) v[h] = z[h];
         butterfly<false>(v, lane);
         sm.reds[warp][hb] = v[0];
         sm.reds[warp][hb + 1] = v[1];
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        const bool last = (t == s.act_end - 1);
         if (warp == 0) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -518,148 +588,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.l_run[h] = sm.l_run[h] * sm.fscale[h] +
                           ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
           }
-          if (last) {
-            // hand the segment's statistics to the epilogue, then reset
-            if (sa > 0 && !warp_wait(&sm.statempty, (sa - 1) & 1, &sm.abort)) {
-              ok = false;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int h = hb + e;
-                sm.stat_m[h] = sm.m_used[h];
-                sm.stat_l[h] = sm.l_run[h];
-                sm.m_used[h] = -INFINITY;
-                sm.l_run[h] = 0.0f;
-              }
-              __syncwarp();
-              mbar_arrive(&sm.statfull);
-            }
-          }
         }
         ++u;
       }
-      ++sa;
-      ok = ok && !sm.abort;
-    }
-    if (!ok) fail(sm, a.status);
-  } else {
-    // ------------------------------------------------------------ epilogue --
-    const int e = threadIdx.x - 128;  // 0..127
-    const int quad = warp - 4;
-    int sa = 0;
-    uint32_t ep = 0;
-    bool ok = true;
-    for (int r = r_first; r <= r_last && ok; ++r) {
-      const Seg s = make_seg(a, g, r);
-      const int pslot = 2 * blockIdx.x + (((long long)r * g.Tq > g.lo) ? 1 : 0);
-      float* po = part_o + (size_t)pslot * kHq * kDv;
-      float* pml = part_ml + (size_t)pslot * kHq * 2;
-      __nv_bfloat16* out = a.out + (size_t)r * kHq * kDv;
-      if (s.active() > 0) {
-        if (!warp_wait(&sm.ofull, sa & 1, &sm.abort) ||
-            !warp_wait(&sm.statfull, sa & 1, &sm.abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int blk = 0; blk < kDv / 128; ++blk) {
-          const int dv = blk * 128 + quad * 32 + lane;
-          for (int half = 0; half < 2; ++half) {
-            uint32_t raw[32];
-            tmem_ld_32cols(tbase + ((uint32_t)(quad * 32) << 16) + kColO + 64 * blk + 32 * half, raw);
-            tmem_wait_ld();
+      if (!ok) break;
+      // ---- finalize the query segment: O out of TMEM ----
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // l_run final
+      if (!warp_wait(&sm.ofull, sa & 1, &sm.abort)) { ok = false; break; }
+      tc_fence_after();
+      for (int blk = 0; blk < kDv / 128; ++blk) {
+        const int dv = blk * 128 + row;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t raw[32];
+          tmem_ld_32cols(tbase + ((uint32_t)(warp * 32) << 16) + kColO + 64 * blk + 32 * half, raw);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int h = 32 * half + i;
-              const float o = __uint_as_float(raw[i]);
-              if (s.complete) {
-                const float l = sm.stat_l[h];
-                out[(size_t)h * kDv + dv] = __float2bfloat16(l > 0.0f ? o / l : 0.0f);
-              } else {
-                po[(size_t)h * kDv + dv] = o;
-              }
+          for (int i = 0; i < 32; ++i) {
+            const int h = 32 * half + i;
+            const float o = __uint_as_float(raw[i]);
+            if (s.complete) {
+              const float l = sm.l_run[h];
+              out[(size_t)h * kDv + dv] = __float2bfloat16(l > 0.0f ? o / l : 0.0f);
+            } else {
+              po[(size_t)h * kDv + dv] = o;
             }
           }
         }
-        if (e < kHq) {
-          const float m = sm.stat_m[e], l = sm.stat_l[e];
-          if (s.complete) {
-            if (a.lse) a.lse[(size_t)r * kHq + e] =
-                l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-          } else {
-            pml[2 * e] = m;
-            pml[2 * e + 1] = l;
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&sm.ofree);
-        mbar_arrive(&sm.statempty);
-        ++sa;
-      } else {
+      }
+      if (row < kHq) {
+        const float m = sm.m_used[row], l = sm.l_run[row];
         if (s.complete) {
-          for (int i = e; i < kHq * kDv; i += 128) out[i] = __float2bfloat16(0.0f);
-          if (a.lse && e < kHq) a.lse[(size_t)r * kHq + e] = -INFINITY;
-        } else if (e < kHq) {
-          pml[2 * e] = -INFINITY;
-          pml[2 * e + 1] = 0.0f;
+          if (a.lse)
+            a.lse[(size_t)r * kHq + row] =
+                l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        } else {
+          pml[2 * row] = m;
+          pml[2 * row + 1] = l;
         }
       }
-      if (!s.complete) {
-        // last CTA to finish this query merges the partials
-        __threadfence();
-        if (!group_sync(&sm.epsync, ep, &sm.abort)) { ok = false; break; }
-        const long long first = (long long)r * g.Tq;
-        const int c0 = g.cta_of(first), c1 = g.cta_of(first + g.Tq - 1);
-        if (e == 0) {
-          const int old = atomicAdd(&counters[r], 1);
-          sm.combine = (old == c1 - c0) ? 1 : 0;
-        }
-        if (!group_sync(&sm.epsync, ep, &sm.abort)) { ok = false; break; }
-        if (sm.combine) {
-          __threadfence();
-          float wsum[kHq];
-          float mmax[kHq];
-#pragma unroll 4
-          for (int h = 0; h < kHq; ++h) {
-            mmax[h] = -INFINITY;
-            wsum[h] = 0.0f;
-          }
-          for (int cc = c0; cc <= c1; ++cc) {
-            const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-            const float* ml = part_ml + (size_t)ps * kHq * 2;
-            for (int h = 0; h < kHq; ++h)
-              if (__ldcg(&ml[2 * h + 1]) > 0.0f) mmax[h] = fmaxf(mmax[h], __ldcg(&ml[2 * h]));
-          }
-          for (int cc = c0; cc <= c1; ++cc) {
-            const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-            const float* ml = part_ml + (size_t)ps * kHq * 2;
-            for (int h = 0; h < kHq; ++h) {
-              const float l = __ldcg(&ml[2 * h + 1]);
-              if (l > 0.0f) wsum[h] += l * exp2f(__ldcg(&ml[2 * h]) - mmax[h]);
-            }
-          }
-          for (int dv = e; dv < kDv; dv += 128) {
-            for (int h = 0; h < kHq; ++h) {
-              float acc = 0.0f;
-              for (int cc = c0; cc <= c1; ++cc) {
-                const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-                const float l = __ldcg(&part_ml[((size_t)ps * kHq + h) * 2 + 1]);
-                if (l > 0.0f) {
-                  const float wgt = exp2f(__ldcg(&part_ml[((size_t)ps * kHq + h) * 2]) - mmax[h]);
-                  acc = fmaf(wgt, __ldcg(&part_o[((size_t)ps * kHq + h) * kDv + dv]), acc);
-                }
-              }
-              out[(size_t)h * kDv + dv] =
-                  __float2bfloat16(wsum[h] > 0.0f ? acc / wsum[h] : 0.0f);
-            }
-          }
-          if (a.lse && e < kHq)
-            a.lse[(size_t)r * kHq + e] =
-                wsum[e] > 0.0f ? (mmax[e] + log2f(wsum[e])) * 0.6931471805599453f : -INFINITY;
-          if (!group_sync(&sm.epsync, ep, &sm.abort)) { ok = false; break; }
-          if (e == 0) counters[r] = 0;
-        }
+      tc_fence_before();
+      mbar_arrive(&sm.ofree);
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // stats read
+      if (row < kHq) {
+        sm.m_used[row] = -INFINITY;
+        sm.l_run[row] = 0.0f;
       }
+      ++sa;
       ok = ok && !sm.abort;
     }
     if (!ok) fail(sm, a.status);
@@ -667,9 +641,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// Merge of the queries whose tiles span several CTAs.  Grid (8 head groups,
+// G): CTA column c handles the query that contains the boundary lo(c) when c
+// is the first boundary inside that query.
+__global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, const float* part_o,
+                                                       const float* part_ml) {
+  const int c = blockIdx.y + 1;
+  const long long bnd = g.lo_of(c);
+  if (bnd % g.Tq == 0) return;
+  const int r = (int)(bnd / g.Tq);
+  const long long first = (long long)r * g.Tq;
+  if (g.lo_of(c - 1) > first) return;  // an earlier boundary of this query merges it
+  const int c0 = g.cta_of(first), c1 = g.cta_of(first + g.Tq - 1);
+  const int h0 = blockIdx.x * 8;
+  __shared__ float wgt[8][kMaxCtas + 1];
+  __shared__ float lsum[8], mmax[8];
+  if (threadIdx.x < 8) {
+    const int h = h0 + threadIdx.x;
+    float M = -INFINITY;
+    for (int cc = c0; cc <= c1; ++cc) {
+      const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+      const float l = part_ml[((size_t)ps * kHq + h) * 2 + 1];
+      if (l > 0.0f) M = fmaxf(M, part_ml[((size_t)ps * kHq + h) * 2]);
+    }
+    float L = 0.0f;
+    for (int cc = c0; cc <= c1; ++cc) {
+      const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+      const float l = part_ml[((size_t)ps * kHq + h) * 2 + 1];
+      const float w = l > 0.0f ? exp2f(part_ml[((size_t)ps * kHq + h) * 2] - M) : 0.0f;
+      wgt[threadIdx.x][cc - c0] = w;
+      L += l * w;
+    }
+    lsum[threadIdx.x] = L;
+    mmax[threadIdx.x] = M;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 8 * kDv; i += 256) {
+    const int hh = i / kDv, dv = i % kDv, h = h0 + hh;
+    float acc = 0.0f;
+    for (int cc = c0; cc <= c1; ++cc) {
+      const float w = wgt[hh][cc - c0];
+      if (w > 0.0f) {
+        const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+        acc = fmaf(w, part_o[((size_t)ps * kHq + h) * kDv + dv], acc);
+      }
+    }
+    const float L = lsum[hh];
+    a.out[((size_t)r * kHq + h) * kDv + dv] = __float2bfloat16(L > 0.0f ? acc / L : 0.0f);
+  }
+  if (a.lse && threadIdx.x < 8) {
+    const float L = lsum[threadIdx.x];
+    a.lse[(size_t)r * kHq + h0 + threadIdx.x] =
+        L > 0.0f ? (mmax[threadIdx.x] + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
 }
 
@@ -681,20 +710,15 @@ bool attn_tc_eligible(const AttnParams& p) {
          (long long)p.lay.nb * p.lay.bs < (1LL << 31) - 1;
 }
 
-size_t attn_tc_ws(int Nq) {
-  const size_t counters = (((size_t)Nq * sizeof(int)) + 255) & ~size_t(255);
-  return kWsHeader + counters + sizeof(float) * 2 * kMaxCtas * kHq * (kDv + 2);
+size_t attn_tc_ws(int) {
+  return kWsHeader + sizeof(float) * 2 * kMaxCtas * kHq * (kDv + 2);
 }
 
 int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
-  CUtensorMap mkv, mq;
-  int rc = make_tmap_2d(&mkv, p.kp, false, kDqk, (uint64_t)p.lay.nb * p.lay.bs, kDqk * 2, 64, 1);
+  CUtensorMap mq;
+  int rc = make_tmap_2d(&mq, p.q, false, kDqk, (uint64_t)p.Nq * kHq, kDqk * 2, 64, kHq);
   if (rc) return rc;
-  rc = make_tmap_2d(&mq, p.q, false, kDqk, (uint64_t)p.Nq * kHq, kDqk * 2, 64, kHq);
-  if (rc) return rc;
-  int* counters = reinterpret_cast<int*>((char*)ws + kWsHeader);
-  const size_t cbytes = (((size_t)p.Nq * sizeof(int)) + 255) & ~size_t(255);
-  float* part_ml = reinterpret_cast<float*>((char*)ws + kWsHeader + cbytes);
+  float* part_ml = reinterpret_cast<float*>((char*)ws + kWsHeader);
   float* part_o = part_ml + (size_t)2 * kMaxCtas * kHq * 2;
   const size_t smem = sizeof(Smem) + 1024;
   static bool attr = false;
@@ -702,13 +726,21 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
     cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  const long long total = (long long)p.Nq * ((p.K + kRows - 1) / kRows);
+  Geo g;
+  g.Tq = (p.K + kRows - 1) / kRows;
+  g.total = (long long)p.Nq * g.Tq;
   long long grid = sm_count();
   if (grid > kMaxCtas) grid = kMaxCtas;
-  if (grid > total) grid = total;
-  k_attn_tc<<<(unsigned)grid, kThreads, smem, s>>>(mkv, mq, p, part_o, part_ml, counters);
+  if (grid > g.total) grid = g.total;
+  g.G = (int)grid;
+  g.lo = g.hi = 0;
+  k_attn_tc<<<(unsigned)grid, kThreads, smem, s>>>(mq, p, part_o, part_ml);
   count_launch();
-  return check_launch("sparse_attn (tensor cores)");
+  rc = check_launch("sparse_attn (tensor cores)");
+  if (rc || grid < 2) return rc;
+  k_attn_tc_merge<<<dim3(kHq / 8, (unsigned)(grid - 1)), 256, 0, s>>>(p, g, part_o, part_ml);
+  count_launch();
+  return check_launch("sparse_attn merge");
 }
 
 }  // namespace dsa

@@ -91,6 +91,10 @@ bool index_score_supported(int dtype, int H, int D);
 size_t index_score_ws(int Nq, int H, int D, long long ld);
 
 int launch_topk(const TopkParams& p, void* ws, size_t ws_bytes, cudaStream_t s);
+// shared-memory block top-K (topk_smem.cu)
+bool topk_smem_eligible(long long ld, int K);
+size_t topk_smem_ws(int Nq, long long ld, int K);
+int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s);
 size_t topk_ws(int Nq, long long ld, int K);
 
 int launch_attn(AttnParams p, bool decode, void* ws, size_t ws_bytes, cudaStream_t s);

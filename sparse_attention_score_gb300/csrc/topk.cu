@@ -54,6 +54,7 @@ __device__ __forceinline__ int block_excl_scan(bool flag, int* sh, int* total) {
 }
 
 // One CTA per row; keys are re-read from global memory (L2) on every pass.
+// Used only for rows too long for the shared-memory block kernel (topk_smem.cu).
 __global__ void __launch_bounds__(kTopkThreads) k_topk_rowwise(TopkParams a) {
   __shared__ int hist[256];
   __shared__ int scan_sh[kWarps + 1];
@@ -158,10 +159,13 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_rowwise(TopkParams a) {
 
 }  // namespace
 
-size_t topk_ws(int, long long, int) { return kWsHeader; }
+size_t topk_ws(int Nq, long long ld, int K) {
+  return kWsHeader + (topk_smem_eligible(ld, K) ? topk_smem_ws(Nq, ld, K) : 0);
+}
 
-int launch_topk(const TopkParams& p, void*, size_t, cudaStream_t s) {
+int launch_topk(const TopkParams& p, void* ws, size_t, cudaStream_t s) {
   if (p.Nq == 0) return DSA_OK;
+  if (topk_smem_eligible(p.ld, p.K)) return launch_topk_smem(p, ws, s);
   k_topk_rowwise<<<p.Nq, kTopkThreads, 0, s>>>(p);
   count_launch();
   return check_launch("topk");

@@ -238,3 +238,26 @@ def test_attention_running_max_rescale_path():
     out_ref, lse_ref = oracle_attn(c, idx)
     assert_out_close(out, lse, out_ref, lse_ref, "rescale")
     assert g.status() == 0
+
+
+@pytest.mark.parametrize("K", [1, 2048, 9000])
+def test_topk_long_rows_ties_across_blocks(K):
+    """Rows longer than one shared-memory block take the block + merge path;
+    heavy ties straddle block boundaries, so the lower-position rule must hold
+    across blocks."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(11 + K)
+    Nq, ld = 5, 150001
+    s = rng.integers(0, 3, size=(Nq, ld)).astype(np.float32)
+    s[1] = rng.standard_normal(ld).astype(np.float32)
+    s[2, :] = 5.0                                  # one value everywhere
+    s[3, 100000:] = 9.0                            # winners all in later blocks
+    n = np.array([150001, 149000, 120000, 150001, 60000], np.int32)
+    st, ne = torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda()
+    idx = torch.empty((Nq, K), dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(dsa.topk_workspace_size(Nq, ld, K))
+    dsa.topk(st, ne, K, idx, ws)
+    got = idx.cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.topk(s, n, K))
+    assert dsa.get_status(ws) == 0
