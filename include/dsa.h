@@ -121,6 +121,21 @@ int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const flo
                     int64_t ld, void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Stage 1, prefill form: all Nq queries belong to sequence `seq` and query r
+ * sits at position q_pos[r] (q_pos NULL: position r).  Same scores as
+ * dsa_index_score with q_seq[r] = seq.  Source: "Day-0 Adaptation of
+ * Trillion-Parameter MoE Models on Domestic GPUs", section 3 (3): the prefill
+ * stage processes the whole prompt at once and is compute-intensive, so the
+ * queries share every key tile (a dense causal contraction on tensor cores).
+ * Errors as for dsa_index_score; seq must be in [0, batch).
+ */
+size_t dsa_index_score_prefill_workspace_size(int Nq, int H_i, int D_i, int64_t ld);
+int dsa_index_score_prefill(const dsa_paged_layout* layout, int seq, const void* q_idx,
+                            const float* w, const void* kidx_pool, int dtype, int H_i, int D_i,
+                            const int32_t* q_pos, int Nq, float* scores, int64_t ld, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Stage 2: top-K selection.
  * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
  * section 3 (1) (Top-K filtering as block-wise scoring, intra-block reduction

@@ -79,6 +79,9 @@ _sig("dsa_last_error_string", ctypes.c_char_p, [])
 _sig("dsa_get_status", _i, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), _i])
 _sig("dsa_index_score_workspace_size", _sz, [_i, _i, _i, _i64])
 _sig("dsa_index_score", _i, [_LP, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _i64, _vp, _sz, _vp])
+_sig("dsa_index_score_prefill_workspace_size", _sz, [_i, _i, _i, _i64])
+_sig("dsa_index_score_prefill", _i, [_LP, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _vp, _i64, _vp, _sz,
+                                     _vp])
 _sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
 _sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
@@ -89,7 +92,9 @@ _sig("dsa_sparse_attn_prefill", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i,
                                      _i, _f, _vp, _vp, _vp, _sz, _vp])
 
 SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_status",
-           "dsa_index_score_workspace_size", "dsa_index_score", "dsa_topk_workspace_size",
+           "dsa_index_score_workspace_size", "dsa_index_score",
+           "dsa_index_score_prefill_workspace_size", "dsa_index_score_prefill",
+           "dsa_topk_workspace_size",
            "dsa_topk", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
            "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill")
 
@@ -186,6 +191,17 @@ def index_score(layout: PagedLayout, q_idx, w, kidx_pool, scores, ws, q_seq=None
     _check(rc, "dsa_index_score")
 
 
+def index_score_prefill(layout: PagedLayout, seq, q_idx, w, kidx_pool, scores, ws, q_pos=None,
+                        stream=None):
+    """scores[Nq, ld] <- indexer scores of Nq queries of sequence `seq`."""
+    Nq, H_i, D_i = q_idx.shape
+    rc = _lib.dsa_index_score_prefill(layout.c(), int(seq), _ptr(q_idx), _ptr(w), _ptr(kidx_pool),
+                                      _elt_dtype(kidx_pool), H_i, D_i, _ptr(q_pos), Nq,
+                                      _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(),
+                                      _stream(stream))
+    _check(rc, "dsa_index_score_prefill")
+
+
 def topk(scores, n_eligible, K, idx, ws, stream=None):
     """idx[Nq, K] <- top-K positions, ascending, -1 padded."""
     Nq, ld = scores.shape
@@ -227,13 +243,17 @@ class Pipeline:
     """The three stages of one decode or prefill step with preallocated buffers.
 
     kind="decode": one query per sequence at position L_b - 1 (q [B, Hq, Dqk]).
-    kind="prefill": Nq queries with explicit q_seq / q_pos.
+    kind="prefill": Nq queries of sequence `prefill_seq` at positions q_pos (the
+    indexer then shares key tiles across queries); prefill_seq=None scores
+    queries of any sequences given by q_seq.
     Buffers (scores, idx, out, lse, workspaces) are allocated once through torch.
     """
 
     def __init__(self, layout: PagedLayout, *, kind: str, Nq: int, Hq: int, Dqk: int, Dv: int,
-                 H_i: int, D_i: int, K: int, ld: Optional[int] = None, device="cuda"):
+                 H_i: int, D_i: int, K: int, ld: Optional[int] = None, device="cuda",
+                 prefill_seq: Optional[int] = 0):
         self.layout, self.kind, self.K = layout, kind, int(K)
+        self.prefill_seq = prefill_seq
         self.Nq, self.Hq, self.Dqk, self.Dv = int(Nq), int(Hq), int(Dqk), int(Dv)
         self.ld = int(ld if ld is not None else max(layout.max_seq_len, 1))
         self.scores = torch.empty((self.Nq, self.ld), dtype=torch.float32, device=device)
@@ -254,8 +274,12 @@ class Pipeline:
             if self.kind != "decode":
                 raise ValueError("prefill needs n_eligible (q_pos + 1)")
             n_eligible = self.layout.seq_lens
-        index_score(self.layout, q_idx, w, kidx_pool, self.scores, self.ws_index, q_seq=q_seq,
-                    q_pos=q_pos, stream=stream)
+        if self.kind == "decode" or self.prefill_seq is None:
+            index_score(self.layout, q_idx, w, kidx_pool, self.scores, self.ws_index, q_seq=q_seq,
+                        q_pos=q_pos, stream=stream)
+        else:
+            index_score_prefill(self.layout, self.prefill_seq, q_idx, w, kidx_pool, self.scores,
+                                self.ws_index, q_pos=q_pos, stream=stream)
         topk(self.scores, n_eligible, self.K, self.idx, self.ws_topk, stream=stream)
         if self.kind == "decode":
             sparse_attn_decode(self.layout, q, k_pool, v_pool, self.idx, sm_scale, self.out,

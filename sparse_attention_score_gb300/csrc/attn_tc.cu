@@ -682,18 +682,28 @@ __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, cons
     mmax[threadIdx.x] = M;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 8 * kDv; i += 256) {
-    const int hh = i / kDv, dv = i % kDv, h = h0 + hh;
-    float acc = 0.0f;
-    for (int cc = c0; cc <= c1; ++cc) {
-      const float w = wgt[hh][cc - c0];
-      if (w > 0.0f) {
-        const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-        acc = fmaf(w, part_o[((size_t)ps * kHq + h) * kDv + dv], acc);
-      }
+  // thread t owns outputs t + 256 k (k < 16): head k/2, dv t + 256 (k & 1);
+  // every slot's 16 loads are independent, so they overlap
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+  for (int cc = c0; cc <= c1; ++cc) {
+    const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+    const float* src = part_o + ((size_t)ps * kHq + h0) * kDv + threadIdx.x;
+    float val[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) val[k] = __ldcg(src + (size_t)(k >> 1) * kDv + 256 * (k & 1));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float w = wgt[k >> 1][cc - c0];
+      acc[k] = w > 0.0f ? fmaf(w, val[k], acc[k]) : acc[k];
     }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int hh = k >> 1, dv = threadIdx.x + 256 * (k & 1);
     const float L = lsum[hh];
-    a.out[((size_t)r * kHq + h) * kDv + dv] = __float2bfloat16(L > 0.0f ? acc / L : 0.0f);
+    a.out[((size_t)r * kHq + h0 + hh) * kDv + dv] = __float2bfloat16(L > 0.0f ? acc[k] / L : 0.0f);
   }
   if (a.lse && threadIdx.x < 8) {
     const float L = lsum[threadIdx.x];

@@ -91,17 +91,19 @@ size_t dsa_index_score_workspace_size(int Nq, int H_i, int D_i, int64_t ld) {
   return index_score_ws(Nq, H_i, D_i, (long long)ld);
 }
 
-int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const float* w,
-                    const void* kidx_pool, int dtype, int H_i, int D_i, const int32_t* q_seq,
-                    const int32_t* q_pos, int Nq, float* scores, int64_t ld, void* ws,
-                    size_t ws_bytes, dsa_stream_t stream) {
+static int index_common(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                        const void* kidx_pool, int dtype, int H_i, int D_i,
+                        const int32_t* q_seq, const int32_t* q_pos, int seq_const, int Nq,
+                        float* scores, int64_t ld, void* ws, size_t ws_bytes,
+                        dsa_stream_t stream) {
   IndexParams p{};
   int rc = check_layout(layout, &p.lay);
   if (rc) return rc;
   if (Nq < 0 || ld < 1) return set_error(DSA_ERR_INVALID, "index_score: Nq < 0 or ld < 1");
-  if (Nq > 65535) return set_error(DSA_ERR_UNSUPPORTED, "index_score: Nq > 65535");
   if (!q_idx || !w || !kidx_pool || !scores)
     return set_error(DSA_ERR_INVALID, "index_score: NULL tensor pointer");
+  if (seq_const >= layout->batch)
+    return set_error(DSA_ERR_INVALID, "index_score_prefill: seq out of range");
   if (!index_score_supported(dtype, H_i, D_i))
     return set_error(DSA_ERR_UNSUPPORTED,
                      "index_score: supported dtype BF16/FP8_E4M3, H_i 1..128, D_i 32/64/128");
@@ -117,11 +119,33 @@ int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const flo
   p.D = D_i;
   p.q_seq = q_seq;
   p.q_pos = q_pos;
+  p.seq_const = seq_const;
   p.Nq = Nq;
   p.scores = scores;
   p.ld = (long long)ld;
   p.status = reinterpret_cast<int*>(ws);
   return launch_index_score(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                    const void* kidx_pool, int dtype, int H_i, int D_i, const int32_t* q_seq,
+                    const int32_t* q_pos, int Nq, float* scores, int64_t ld, void* ws,
+                    size_t ws_bytes, dsa_stream_t stream) {
+  return index_common(layout, q_idx, w, kidx_pool, dtype, H_i, D_i, q_seq, q_pos, -1, Nq, scores,
+                      ld, ws, ws_bytes, stream);
+}
+
+size_t dsa_index_score_prefill_workspace_size(int Nq, int H_i, int D_i, int64_t ld) {
+  return index_score_ws(Nq, H_i, D_i, (long long)ld);
+}
+
+int dsa_index_score_prefill(const dsa_paged_layout* layout, int seq, const void* q_idx,
+                            const float* w, const void* kidx_pool, int dtype, int H_i, int D_i,
+                            const int32_t* q_pos, int Nq, float* scores, int64_t ld, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream) {
+  if (seq < 0) return set_error(DSA_ERR_INVALID, "index_score_prefill: seq < 0");
+  return index_common(layout, q_idx, w, kidx_pool, dtype, H_i, D_i, nullptr, q_pos, seq, Nq,
+                      scores, ld, ws, ws_bytes, stream);
 }
 
 size_t dsa_topk_workspace_size(int Nq, int64_t ld, int K) {

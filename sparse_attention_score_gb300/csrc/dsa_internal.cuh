@@ -32,6 +32,7 @@ struct IndexParams {
   int dtype, H, D;
   const int32_t* q_seq;
   const int32_t* q_pos;
+  int seq_const;  // >= 0: every query belongs to this sequence (q_seq ignored)
   int Nq;
   float* scores;
   long long ld;
@@ -87,6 +88,9 @@ int launch_index_score(const IndexParams& p, cudaStream_t s);
 // tensor-core indexer (FP8 E4M3, H_i = 64, D_i = 128, block size 64)
 bool index_tc_eligible(const IndexParams& p);
 int launch_index_tc(const IndexParams& p, cudaStream_t s);
+// tensor-core prefill indexer (queries of one sequence sharing key tiles)
+bool index_prefill_tc_eligible(const IndexParams& p);
+int launch_index_prefill_tc(const IndexParams& p, cudaStream_t s);
 bool index_score_supported(int dtype, int H, int D);
 size_t index_score_ws(int Nq, int H, int D, long long ld);
 

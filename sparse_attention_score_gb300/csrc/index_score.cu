@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams
 
   const long long p = (long long)blockIdx.x * kGenThreads + threadIdx.x;
   if (p >= a.ld) return;
-  const int b = a.q_seq ? __ldg(&a.q_seq[r]) : r;
+  const int b = a.seq_const >= 0 ? a.seq_const : (a.q_seq ? __ldg(&a.q_seq[r]) : r);
   float out = -INFINITY;
   if (b >= 0 && b < a.lay.batch) {
     long long L = __ldg(&a.lay.seq_lens[b]);
@@ -135,7 +135,9 @@ size_t index_score_ws(int, int, int, long long) { return kWsHeader; }
 
 int launch_index_score(const IndexParams& p, cudaStream_t s) {
   if (p.Nq == 0) return DSA_OK;
-  if (index_tc_eligible(p)) return launch_index_tc(p, s);
+  if (p.seq_const >= 0 && index_prefill_tc_eligible(p)) return launch_index_prefill_tc(p, s);
+  if (p.seq_const < 0 && index_tc_eligible(p)) return launch_index_tc(p, s);
+  if (p.Nq > 65535) return set_error(DSA_ERR_UNSUPPORTED, "index_score: Nq > 65535 for this shape");
   if (p.dtype == DSA_BF16) {
     if (p.D == 32) return launch_generic<32, DSA_BF16>(p, s);
     if (p.D == 64) return launch_generic<64, DSA_BF16>(p, s);

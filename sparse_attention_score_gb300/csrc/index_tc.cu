@@ -60,7 +60,7 @@ struct Query {
 
 __device__ __forceinline__ Query query_info(const IndexParams& a, int r) {
   Query q{-1, 0};
-  const int b = a.q_seq ? __ldg(&a.q_seq[r]) : r;
+  const int b = a.seq_const >= 0 ? a.seq_const : (a.q_seq ? __ldg(&a.q_seq[r]) : r);
   if (b < 0 || b >= a.lay.batch) return q;
   long long L = __ldg(&a.lay.seq_lens[b]);
   const long long cap = (long long)a.lay.maxb * a.lay.bs;

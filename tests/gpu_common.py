@@ -58,10 +58,18 @@ class GpuRun:
 
     def scores(self):
         d, p = self.d, self.pipe
-        qs = None if self.case.kind == "decode" else d.q_seq
-        qp = None if self.case.kind == "decode" else d.q_pos
+        if self.case.kind == "decode":
+            self.dsa.index_score(self.layout, d.q_idx, d.w, d.kidx_pool, p.scores, p.ws_index)
+        else:
+            self.dsa.index_score_prefill(self.layout, 0, d.q_idx, d.w, d.kidx_pool, p.scores,
+                                         p.ws_index, q_pos=d.q_pos)
+        return p.scores
+
+    def scores_general(self):
+        """The general entry point (explicit q_seq) on the same inputs."""
+        d, p = self.d, self.pipe
         self.dsa.index_score(self.layout, d.q_idx, d.w, d.kidx_pool, p.scores, p.ws_index,
-                             q_seq=qs, q_pos=qp)
+                             q_seq=d.q_seq, q_pos=d.q_pos)
         return p.scores
 
     def topk(self, scores=None, n_elig=None):

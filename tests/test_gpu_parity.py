@@ -261,3 +261,29 @@ def test_topk_long_rows_ties_across_blocks(K):
     got = idx.cpu().numpy()
     np.testing.assert_array_equal(got, oracle.topk(s, n, K))
     assert dsa.get_status(ws) == 0
+
+
+def test_prefill_indexer_both_entry_points():
+    """The prefill form (queries of one sequence sharing key tiles) and the
+    general form (explicit q_seq) give the oracle's scores bit for bit."""
+    need_gpu()
+    c = W.make_case("prefill-idx", seed=990, kind="prefill", T=1300, K=256, **LAT_SHAPES)
+    g = GpuRun(c)
+    s_ref = oracle_scores(c)
+    assert_scores_equal(g.scores().cpu().numpy(), s_ref, c.n_elig)
+    assert_scores_equal(g.scores_general().cpu().numpy(), s_ref, c.n_elig)
+    assert g.status() == 0
+
+
+def test_prefill_indexer_query_subset_ragged_block():
+    """37 queries at scattered positions (a ragged last block of 16)."""
+    need_gpu()
+    rows = np.sort(np.random.default_rng(4).choice(3000, 37, replace=False))
+    c = W.make_case("prefill-sub", seed=991, kind="prefill", T=3000, K=512, q_rows=rows,
+                    **LAT_SHAPES)
+    g = GpuRun(c)
+    s_ref = oracle_scores(c)
+    assert_scores_equal(g.scores().cpu().numpy(), s_ref, c.n_elig)
+    idx = g.topk().cpu().numpy()
+    np.testing.assert_array_equal(idx, oracle.topk(s_ref, c.n_elig, c.K))
+    assert g.status() == 0
