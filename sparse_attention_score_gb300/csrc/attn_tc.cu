@@ -29,8 +29,9 @@
 // Warp roles (288 threads):
 //   warps 0-3 softmax, and at the end of each query segment O out of TMEM;
 //   warps 4-7 producer: Q by TMA; per tile the 9 K chunks and, one tile
-//   later, the 8 V chunks again, one row per thread, 16-byte cp.async into
-//   the 128-byte swizzled layout (rows of 1152 bytes anywhere in the pool);
+//   later, the 8 V chunks again, by 16-byte cp.async into the 128-byte
+//   swizzled layout, 8 consecutive threads per 128-byte row chunk (rows of
+//   1152 bytes anywhere in the pool);
 //   warp 8 TMEM owner and MMA issuer.  QK of tile i is issued before PV of
 //   tile i-1, so the softmax of one tile overlaps the MMAs of the next.
 // Selected rows that are padding, past the sequence, non-causal or behind a
@@ -69,7 +70,8 @@ struct __align__(1024) Smem {
   uint8_t phi[kPBytes];  // P^T, bf16 part
   uint8_t plo[kPBytes];  // P^T, bf16 remainder (P - phi)
   uint64_t qfull, qempty, full[kRing], empty[kRing], sfull[2], sempty[2], pfull, pempty;
-  uint64_t ofull, ofree, smsync, done;
+  uint64_t ofull, ofree, smsync, prsync, done;
+  int rowtab[2][kRows];  // physical rows of the producer's current / previous tile
   uint32_t tmem_base;
   int abort;
   int rescale[2];
@@ -270,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.ofull, 1);
     mbar_init(&sm.ofree, 128);
     mbar_init(&sm.smsync, 128);
+    mbar_init(&sm.prsync, 128);
     mbar_init(&sm.done, 1);
     fence_mbar_init();
   }
@@ -289,13 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ producer --
-    // Thread `row` copies row `row` of every chunk of every tile: 8 x 16 B per
-    // 64-dim chunk, placed in the 128-byte swizzled K-major layout.
-    const int row = threadIdx.x - 128;
+    // Each 128-byte row chunk is copied by 8 consecutive threads (16 B each),
+    // so a warp instruction moves four whole rows; thread t copies granule
+    // t % 8 of rows t / 8 + 16 i.  The tile's physical rows are looked up
+    // once (thread t: row t) into a shared table.
+    const int pt = threadIdx.x - 128;
+    const int gq = pt & 7, r0 = pt >> 3;
     const char* kv = reinterpret_cast<const char*>(a.kp);
     int j = 0;            // pairs issued
     int signalled = 0;    // pairs signalled full
-    int sa = 0;
+    int sa = 0, u = 0;
+    uint32_t ps = 0;
     bool ok = true;
     auto signal_one = [&]() {
       fence_proxy_async_smem();
@@ -306,18 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_wait<0>();
       while (signalled < j) signal_one();
     };
-    auto issue_pair = [&](int c0, int nc, long long prow) -> bool {
+    auto issue_pair = [&](int c0, int nc, const int* rows) -> bool {
       const int slot = j % kRing;
       const uint32_t par = ((j / kRing) & 1) ^ 1;
       if (!warp_wait(&sm.empty[slot], par, &sm.abort)) return false;
-      const uint32_t nbytes = prow >= 0 ? 16u : 0u;
-      const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) : kv;
-      uint8_t* dst = sm.ring[slot] + row * 128;
-      for (int i = 0; i < nc; ++i) {
-#pragma unroll
-        for (int gq = 0; gq < 8; ++gq)
-          cp_async16(dst + i * kChunkBytes + ((gq ^ (row & 7)) << 4),
-                     src + (c0 + i) * 128 + (prow >= 0 ? gq * 16 : 0), nbytes);
+      uint8_t* base = sm.ring[slot];
+#pragma unroll 2
+      for (int i = 0; i < kRows / 16; ++i) {
+        const int r = r0 + 16 * i;
+        const int prow = rows[r];
+        const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + gq * 16 : kv;
+        const uint32_t nbytes = prow >= 0 ? 16u : 0u;
+        uint8_t* dst = base + r * 128 + ((gq ^ (r & 7)) << 4);
+        for (int cc = 0; cc < nc; ++cc)
+          cp_async16(dst + cc * kChunkBytes, src + (prow >= 0 ? (c0 + cc) * 128 : 0), nbytes);
       }
       cp_async_commit();
       ++j;
@@ -330,15 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walker w;
     w.init(a, g, r_first, r_last);
     int cur_r = -1;
-    long long prev_row = -1;
     bool have_prev = false;
-    int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + row) : -1;
+    int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + pt) : -1;
     while (w.ok && ok) {
       if (w.r != cur_r) {
         // new query: drain, wait for the previous Q to be consumed, load Q
         flush();
         bool qok = true;
-        if (threadIdx.x == 128) {
+        if (pt == 0) {
           if (sa > 0) qok = mbar_wait(&sm.qempty, (sa - 1) & 1, &sm.abort);
           if (qok) {
             mbar_arrive_expect_tx(&sm.qfull, kQChunks * kQChunkBytes);
@@ -350,21 +358,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_r = w.r;
         ++sa;
       }
+      // this tile's rows into the table (the slot read last by the previous
+      // tile's V copies is free once every producer thread is past them)
       const long long row_cur = pos_row(a, w.s, p_cur, false);
-      // look one tile ahead for the position this thread copies next
       Walker nx = w;
       nx.next(a, g);
-      const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + row) : -1;
-      for (int c = 0; c < kQChunks && ok; c += 2) ok = issue_pair(c, min(2, kQChunks - c), row_cur);
+      const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + pt) : -1;
+      if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
+      sm.rowtab[u & 1][pt] = (int)row_cur;
+      if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
+      for (int c = 0; c < kQChunks && ok; c += 2)
+        ok = issue_pair(c, min(2, kQChunks - c), sm.rowtab[u & 1]);
       if (ok && have_prev)
-        for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, prev_row);
-      prev_row = row_cur;
+        for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, sm.rowtab[(u - 1) & 1]);
       have_prev = true;
       p_cur = p_next;
       w = nx;
+      ++u;
     }
     if (ok && have_prev)
-      for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, prev_row);
+      for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, sm.rowtab[(u - 1) & 1]);
     flush();
     if (!ok) fail(sm, a.status);
   } else if (warp == 8) {
@@ -475,9 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      // validity of this thread's row is looked up one tile ahead
+      bool valid_next = pos_row(a, s, sel_pos(a, s, (long long)s.t0 * kRows + row), true) >= 0;
       for (int t = s.t0; t < s.act_end; ++t) {
-        const bool valid =
-            pos_row(a, s, sel_pos(a, s, (long long)t * kRows + row), true) >= 0;
+        const bool valid = valid_next;
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         float z[kHq], v[kHq];
@@ -574,6 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.pfull);
+        if (t + 1 < s.act_end)
+          valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
         // per-head tile sum of the probabilities as the MMA sees them
 #pragma unroll
         for (int h = 0; h < kHq; ++h) v[h] = z[h];

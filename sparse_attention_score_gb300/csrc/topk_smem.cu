@@ -75,9 +75,23 @@ __device__ __forceinline__ void radix_pass(const uint32_t* keys, int cnt, int sh
   const int nb = 1 << bits;
   for (int i = threadIdx.x; i < nb; i += kThreads) sh.hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < cnt; i += kThreads) {
-    const uint32_t k = keys[i];
-    if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & (uint32_t)(nb - 1)], 1);
+  // Scores concentrate in a few digits (integer scores share an exponent), so
+  // equal bins of a warp are combined first: one shared atomic per distinct bin.
+  const int lane = threadIdx.x & 31;
+  for (int base = 0; base < cnt; base += kThreads) {
+    const int i = base + threadIdx.x;
+    uint32_t k = 0;
+    bool m = false;
+    if (i < cnt) {
+      k = keys[i];
+      m = (k & mask) == prefix;
+    }
+    const unsigned active = __ballot_sync(0xffffffffu, m);
+    if (m) {
+      const uint32_t bin = (k >> shift) & (uint32_t)(nb - 1);
+      const unsigned peers = __match_any_sync(active, bin);
+      if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], __popc(peers));
+    }
   }
   __syncthreads();
   // thread t owns bins nb-1-2t and nb-2-2t (highest digits first)
