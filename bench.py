@@ -15,7 +15,7 @@ timed replay a 512 MiB buffer is written to flush L2 (outside the timed
 region); each replay is bracketed by CUDA events on the stream the kernels run
 on, with a barrier and a synchronize on both sides of the timed loop; the
 reported time is the max over ranks.  Per-stage times come from the stage
-graphs replayed back to back with events between them.  With N GPUs (torchrun) every rank runs its own batch
+graphs, each replayed on its own right after the flush.  With N GPUs (torchrun) every rank runs its own batch
 (weak scaling, no data-path collective).
 
 --impl reference times the CPU oracle (test infrastructure, one thread) on a
@@ -238,20 +238,20 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     step_ms = np.array([a_.elapsed_time(b_) for a_, b_ in ev])
     total_ms = float(step_ms.sum())
     launches = launches_per["step"] * steps
-    # per-stage device time: the stage graphs replayed back to back, events between
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    for i in range(steps):
-        flush.fill_(float(i))
-        sev[i][0].record(stream)
-        graphs["index_score"].replay()
-        sev[i][1].record(stream)
-        graphs["topk"].replay()
-        sev[i][2].record(stream)
-        graphs["sparse_attn"].replay()
-        sev[i][3].record(stream)
-    torch.cuda.synchronize()
-    stage = np.array([[sev[i][k].elapsed_time(sev[i][k + 1]) for k in range(3)]
-                      for i in range(steps)])
+    # per-stage device time: each stage graph replayed on its own, right after
+    # the L2 flush kernel (which keeps the GPU busy while the host submits the
+    # replay, so no host gap lands between the events)
+    stage = np.zeros((steps, 3))
+    for k, name_ in enumerate(("index_score", "topk", "sparse_attn")):
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            sev[i][0].record(stream)
+            graphs[name_].replay()
+            sev[i][1].record(stream)
+        torch.cuda.synchronize()
+        stage[:, k] = [a_.elapsed_time(b_) for a_, b_ in sev]
     status = pipe.status()
 
     e2e = None

@@ -28,6 +28,8 @@ template <int HPW, int DVL>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int Hq = a.Hq, Dqk = a.Dqk, Dv = a.Dv;
+  grid_dependency_wait();
+  launch_dependents();
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smraw);          // [Hq][Dqk]
   float* krow = reinterpret_cast<float*>(smraw + (size_t)Hq * Dqk * 2);  // [Dqk]
   float* vrow = krow + Dqk;                                               // [Dv]
@@ -143,6 +145,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
 
 // grid (Hq, Nq): merge the S partials of one (query, head).
 __global__ void __launch_bounds__(128) k_attn_combine(AttnParams a) {
+  grid_dependency_wait();
+  launch_dependents();
   const int h = blockIdx.x, r = blockIdx.y, S = a.S, Hq = a.Hq, Dv = a.Dv;
   __shared__ float wsh[64];
   __shared__ float lsum_sh, mmax_sh;

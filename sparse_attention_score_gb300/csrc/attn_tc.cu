@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   g.hi = g.lo_of(blockIdx.x + 1);
   const int r_first = (int)(g.lo / g.Tq);
   const int r_last = g.hi > g.lo ? (int)((g.hi - 1) / g.Tq) : r_first - 1;
+  launch_dependents();
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -289,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  grid_dependency_wait();  // everything below reads inputs of earlier kernels
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ producer --
@@ -668,6 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // is the first boundary inside that query.
 __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, const float* part_o,
                                                        const float* part_ml) {
+  grid_dependency_wait();
+  launch_dependents();
   const int c = blockIdx.y + 1;
   const long long bnd = g.lo_of(c);
   if (bnd % g.Tq == 0) return;
@@ -760,12 +764,16 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   if (grid > g.total) grid = g.total;
   g.G = (int)grid;
   g.lo = g.hi = 0;
-  k_attn_tc<<<(unsigned)grid, kThreads, smem, s>>>(mq, p, part_o, part_ml);
+  cudaError_t e =
+      launch_pdl(k_attn_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mq, p, part_o, part_ml);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   rc = check_launch("sparse_attn (tensor cores)");
   if (rc || grid < 2) return rc;
-  k_attn_tc_merge<<<dim3(kHq / 8, (unsigned)(grid - 1)), 256, 0, s>>>(p, g, part_o, part_ml);
+  e = launch_pdl(k_attn_tc_merge, dim3(kHq / 8, (unsigned)(grid - 1)), dim3(256), 0, s, p, g,
+                 (const float*)part_o, (const float*)part_ml);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("sparse_attn merge");
 }
 

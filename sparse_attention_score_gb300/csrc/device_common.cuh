@@ -9,6 +9,18 @@
 
 namespace dsa {
 
+// Programmatic dependent launch: kernels of this library are launched so that
+// the next kernel in the stream may start while this one finishes.  A kernel
+// lets its dependents start with launch_dependents() and, before it reads any
+// global memory another kernel may have written, waits for the previous grid
+// with grid_dependency_wait() (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(int* status, int bit) {
   if (status) atomicOr(status, bit);
 }

@@ -71,6 +71,24 @@ struct AttnParams {
   int S;           // splits of the K selected rows
 };
 
+// Launch with the programmatic-stream-serialization attribute (the kernel must
+// call grid_dependency_wait() before reading inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // host-side bookkeeping (dsa_api.cu)
 void count_launch(int n = 1);
 int set_error(int code, const std::string& msg);

@@ -81,29 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblocks = (a.Nq + kQB - 1) / kQB;
-  const int b = a.seq_const;
-  long long L = 0;
-  if (b >= 0 && b < a.lay.batch) {
-    L = __ldg(&a.lay.seq_lens[b]);
-    const long long cap = (long long)a.lay.maxb * a.lay.bs;
-    if (L > cap || L > a.ld) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) flag_status(a.status, DSA_STATUS_BAD_LENGTH);
-      L = L < cap ? L : cap;
-      L = L < a.ld ? L : a.ld;
-    }
-  } else if (blockIdx.x == 0 && threadIdx.x == 0) {
-    flag_status(a.status, DSA_STATUS_BAD_INDEX);
-  }
-
-  // key tiles per query block (the block's largest eligible count)
-  for (int bi = threadIdx.x; bi < nblocks; bi += kThreads) {
-    long long n = 0;
-    for (int j = 0; j < kQB; ++j) {
-      const long long e = elig(a, L, bi * kQB + j);
-      n = e > n ? e : n;
-    }
-    s.prefix[bi + 1] = (int)((n + kTileRows - 1) / kTileRows);
-  }
+  launch_dependents();
   if (threadIdx.x == 0) {
     s.prefix[0] = 0;
     s.abort = 0;
@@ -128,6 +106,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_q);
+  }
+  grid_dependency_wait();  // inputs below may come from the previous kernel
+  const int b = a.seq_const;
+  long long L = 0;
+  if (b >= 0 && b < a.lay.batch) {
+    L = __ldg(&a.lay.seq_lens[b]);
+    const long long cap = (long long)a.lay.maxb * a.lay.bs;
+    if (L > cap || L > a.ld) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) flag_status(a.status, DSA_STATUS_BAD_LENGTH);
+      L = L < cap ? L : cap;
+      L = L < a.ld ? L : a.ld;
+    }
+  } else if (blockIdx.x == 0 && threadIdx.x == 0) {
+    flag_status(a.status, DSA_STATUS_BAD_INDEX);
+  }
+
+  // key tiles per query block (the block's largest eligible count)
+  for (int bi = threadIdx.x; bi < nblocks; bi += kThreads) {
+    long long n = 0;
+    for (int j = 0; j < kQB; ++j) {
+      const long long e = elig(a, L, bi * kQB + j);
+      n = e > n ? e : n;
+    }
+    s.prefix[bi + 1] = (int)((n + kTileRows - 1) / kTileRows);
   }
   __syncthreads();
   if (warp == 0) {
@@ -361,8 +363,10 @@ int launch_index_prefill_tc(const IndexParams& p, cudaStream_t s) {
   long long grid = sm_count();
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  k_index_prefill_tc<<<(unsigned)grid, kThreads, smem, s>>>(mk, mq, p);
+  const cudaError_t e =
+      launch_pdl(k_index_prefill_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mk, mq, p);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("index_score prefill (tensor cores)");
 }
 

@@ -65,6 +65,8 @@ template <int D, int DT>
 __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams a) {
   extern __shared__ float sm[];
   const int H = a.H;
+  grid_dependency_wait();
+  launch_dependents();
   const int r = blockIdx.y;
   float* qs = sm;
   float* ws = sm + H * D;

@@ -101,21 +101,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.Nq;
+  launch_dependents();
 
-  // tiles per query, then an exclusive prefix (one warp)
-  for (int r = threadIdx.x; r < nq; r += kThreads) {
-    const Query q = query_info(a, r);
-    s.prefix[r + 1] = (int)((q.n + kTileRows - 1) / kTileRows);
-    if (blockIdx.x == 0) {
-      if (q.b < 0) {
-        flag_status(a.status, DSA_STATUS_BAD_INDEX);
-      } else {
-        const long long L = __ldg(&a.lay.seq_lens[q.b]);
-        if (L > (long long)a.lay.maxb * a.lay.bs || L > a.ld)
-          flag_status(a.status, DSA_STATUS_BAD_LENGTH);
-      }
-    }
-  }
   if (threadIdx.x == 0) {
     s.prefix[0] = 0;
     s.abort = 0;
@@ -139,6 +126,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_q);
+  }
+  grid_dependency_wait();  // inputs below may come from the previous kernel
+  // tiles per query, then an exclusive prefix (one warp)
+  for (int r = threadIdx.x; r < nq; r += kThreads) {
+    const Query q = query_info(a, r);
+    s.prefix[r + 1] = (int)((q.n + kTileRows - 1) / kTileRows);
+    if (blockIdx.x == 0) {
+      if (q.b < 0) {
+        flag_status(a.status, DSA_STATUS_BAD_INDEX);
+      } else {
+        const long long L = __ldg(&a.lay.seq_lens[q.b]);
+        if (L > (long long)a.lay.maxb * a.lay.bs || L > a.ld)
+          flag_status(a.status, DSA_STATUS_BAD_LENGTH);
+      }
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -365,8 +367,9 @@ int launch_index_tc(const IndexParams& p, cudaStream_t s) {
   long long grid = 2LL * sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid < 1) grid = 1;
-  k_index_tc<<<(unsigned)grid, kThreads, smem, s>>>(mk, mq, p);
+  const cudaError_t e = launch_pdl(k_index_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mk, mq, p);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("index_score (tensor cores)");
 }
 

@@ -57,6 +57,8 @@ __device__ __forceinline__ int block_excl_scan(bool flag, int* sh, int* total) {
 // Used only for rows too long for the shared-memory block kernel (topk_smem.cu).
 __global__ void __launch_bounds__(kTopkThreads) k_topk_rowwise(TopkParams a) {
   __shared__ int hist[256];
+  grid_dependency_wait();
+  launch_dependents();
   __shared__ int scan_sh[kWarps + 1];
   __shared__ uint32_t sel_digit;
   __shared__ int sel_above;

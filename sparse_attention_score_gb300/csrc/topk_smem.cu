@@ -206,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_topk_block(TopkParams a, int nchunks, uint32_t* cand_key, int32_t* cand_pos, int* cand_cnt) {
   extern __shared__ uint32_t keys[];
   __shared__ Shared sh;
+  grid_dependency_wait();
+  launch_dependents();
   const int r = kMode == 2 ? blockIdx.x : blockIdx.y;
   const int c = kMode == 2 ? 0 : blockIdx.x;
   long long n = __ldg(&a.n_elig[r]);
@@ -306,8 +308,10 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   const size_t smem = kCap * sizeof(uint32_t);
   if (nch == 1) {
     set_smem_attr<0>();
-    k_topk_block<0><<<dim3(1, p.Nq), kThreads, smem, s>>>(p, 1, nullptr, nullptr, nullptr);
+    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem, s, p, 1,
+                                     (uint32_t*)nullptr, (int32_t*)nullptr, (int*)nullptr);
     count_launch();
+    if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
     return check_launch("topk");
   }
   char* base = (char*)ws + kWsHeader;
@@ -317,12 +321,15 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   int* ccnt = reinterpret_cast<int*>(base + nslot * p.K * 8);
   set_smem_attr<1>();
   set_smem_attr<2>();
-  k_topk_block<1><<<dim3(nch, p.Nq), kThreads, smem, s>>>(p, nch, ckey, cpos, ccnt);
+  cudaError_t e = launch_pdl(k_topk_block<1>, dim3(nch, p.Nq), dim3(kThreads), smem, s, p, nch,
+                             ckey, cpos, ccnt);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   int rc = check_launch("topk (blocks)");
   if (rc) return rc;
-  k_topk_block<2><<<p.Nq, kThreads, smem, s>>>(p, nch, ckey, cpos, ccnt);
+  e = launch_pdl(k_topk_block<2>, dim3(p.Nq), dim3(kThreads), smem, s, p, nch, ckey, cpos, ccnt);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("topk (merge)");
 }
 
