@@ -26,14 +26,16 @@
 // partial (O, m, l) per CTA in the workspace and a second small kernel merges
 // them:  M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
 //
-// Warp roles (288 threads):
+// Warp roles (320 threads):
 //   warps 0-3 softmax, and at the end of each query segment O out of TMEM;
-//   warps 4-7 producer: Q by TMA; per tile the 9 K chunks and, one tile
-//   later, the 8 V chunks again, by 16-byte cp.async into the 128-byte
-//   swizzled layout, 8 consecutive threads per 128-byte row chunk (rows of
-//   1152 bytes anywhere in the pool);
-//   warp 8 TMEM owner and MMA issuer.  QK of tile i is issued before PV of
-//   tile i-1, so the softmax of one tile overlaps the MMAs of the next.
+//   warps 4-7 producer: the tile's 9 chunks of 128 rows by 16-byte cp.async
+//   into the 128-byte swizzled layout, 8 consecutive threads per 128-byte
+//   row chunk (rows of 1152 bytes anywhere in the pool); the tile stays
+//   resident from QK to PV, each chunk slot refilled for the next tile as
+//   soon as its last MMA is done (chunk 8 right after QK, chunks 0-7 after
+//   their PV block);
+//   warp 8 TMEM owner and MMA issuer; warp 9 streams Q's chunks from L2 by
+//   TMA through a three-slot ring.
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
@@ -49,13 +51,12 @@ using namespace sm100;
 
 constexpr int kHq = 64, kDqk = 576, kDv = 512;
 constexpr int kRows = 128;
+constexpr int kChunks = kDqk / 64;           // 9 K chunks of 64 dims; the first 8 are V
 constexpr int kChunkBytes = kRows * 128;     // 64 dims x 128 rows, bf16
-constexpr int kPairBytes = 2 * kChunkBytes;  // two chunks at a fixed 16 KB stride
-constexpr int kRing = 3;                     // pair slots
-constexpr int kQChunks = kDqk / 64;          // 9
+constexpr int kQRing = 3;                    // Q chunks in flight
 constexpr int kQChunkBytes = kHq * 128;      // 8 KB
 constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
-constexpr int kThreads = 288;                // 4 softmax + 4 producer + 1 MMA warps
+constexpr int kThreads = 320;                // 4 softmax + 4 producer + MMA + Q loader warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
 constexpr uint32_t kColO = 128;  // four 64-column O^T blocks
@@ -63,15 +64,18 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxCtas = 160;
 constexpr uint32_t kIdescQK = instr_desc(128, kHq, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
+// Chunk order within a tile: chunk 8 (needed by QK only) first, because its
+// slot is the first one the previous tile releases.
+__device__ __forceinline__ int chunk_at(int i) { return i == 0 ? 8 : i - 1; }
 
 struct __align__(1024) Smem {
-  uint8_t q[kQChunks][kQChunkBytes];
-  uint8_t ring[kRing][kPairBytes];
-  uint8_t phi[kPBytes];  // P^T, bf16 part
-  uint8_t plo[kPBytes];  // P^T, bf16 remainder (P - phi)
-  uint64_t qfull, qempty, full[kRing], empty[kRing], sfull[2], sempty[2], pfull, pempty;
-  uint64_t ofull, ofree, smsync, prsync, done;
-  int rowtab[2][kRows];  // physical rows of the producer's current / previous tile
+  uint8_t kv[kChunks][kChunkBytes];  // the tile's rows, resident from QK to PV
+  uint8_t q[kQRing][kQChunkBytes];   // Q chunks streamed from L2
+  uint8_t phi[kPBytes];              // P^T, bf16 part
+  uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi)
+  uint64_t kfull[kChunks], kempty[kChunks], qfull[kQRing], qempty[kQRing];
+  uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done;
+  int rowtab[kRows];  // physical rows of the producer's current tile
   uint32_t tmem_base;
   int abort;
   int rescale[2];
@@ -258,11 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     sm.abort = 0;
     sm.rescale[0] = sm.rescale[1] = 0;
-    mbar_init(&sm.qfull, 1);
-    mbar_init(&sm.qempty, 1);
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(&sm.full[i], 128);
-      mbar_init(&sm.empty[i], 1);
+    for (int i = 0; i < kChunks; ++i) {
+      mbar_init(&sm.kfull[i], 128);
+      mbar_init(&sm.kempty[i], 1);
+    }
+    for (int i = 0; i < kQRing; ++i) {
+      mbar_init(&sm.qfull[i], 1);
+      mbar_init(&sm.qempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.sfull[i], 1);
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) tma_prefetch_desc(&map_q);
+  if (warp == 9 && lane == 0) tma_prefetch_desc(&map_q);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,171 +303,141 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each 128-byte row chunk is copied by 8 consecutive threads (16 B each),
     // so a warp instruction moves four whole rows; thread t copies granule
     // t % 8 of rows t / 8 + 16 i.  The tile's physical rows are looked up
-    // once (thread t: row t) into a shared table.
+    // once (thread t: row t) into a shared table.  Up to four chunks are in
+    // flight per thread before the oldest is waited for and signalled.
     const int pt = threadIdx.x - 128;
     const int gq = pt & 7, r0 = pt >> 3;
     const char* kv = reinterpret_cast<const char*>(a.kp);
-    int j = 0;            // pairs issued
-    int signalled = 0;    // pairs signalled full
-    int sa = 0, u = 0;
     uint32_t ps = 0;
     bool ok = true;
-    auto signal_one = [&]() {
+    int pend_c[kChunks];
+    int npend = 0, head = 0;
+    auto signal_oldest = [&]() {
       fence_proxy_async_smem();
-      mbar_arrive(&sm.full[signalled % kRing]);
-      ++signalled;
-    };
-    auto flush = [&]() {
-      cp_async_wait<0>();
-      while (signalled < j) signal_one();
-    };
-    auto issue_pair = [&](int c0, int nc, const int* rows) -> bool {
-      const int slot = j % kRing;
-      const uint32_t par = ((j / kRing) & 1) ^ 1;
-      if (!warp_wait(&sm.empty[slot], par, &sm.abort)) return false;
-      uint8_t* base = sm.ring[slot];
-#pragma unroll 2
-      for (int i = 0; i < kRows / 16; ++i) {
-        const int r = r0 + 16 * i;
-        const int prow = rows[r];
-        const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + gq * 16 : kv;
-        const uint32_t nbytes = prow >= 0 ? 16u : 0u;
-        uint8_t* dst = base + r * 128 + ((gq ^ (r & 7)) << 4);
-        for (int cc = 0; cc < nc; ++cc)
-          cp_async16(dst + cc * kChunkBytes, src + (prow >= 0 ? (c0 + cc) * 128 : 0), nbytes);
-      }
-      cp_async_commit();
-      ++j;
-      if (j - signalled > 2) {
-        cp_async_wait<2>();
-        signal_one();
-      }
-      return true;
+      mbar_arrive(&sm.kfull[pend_c[head]]);
+      head = (head + 1) % kChunks;
+      --npend;
     };
     Walker w;
     w.init(a, g, r_first, r_last);
-    int cur_r = -1;
-    bool have_prev = false;
+    int u = 0;
     int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + pt) : -1;
     while (w.ok && ok) {
-      if (w.r != cur_r) {
-        // new query: drain, wait for the previous Q to be consumed, load Q
-        flush();
-        bool qok = true;
-        if (pt == 0) {
-          if (sa > 0) qok = mbar_wait(&sm.qempty, (sa - 1) & 1, &sm.abort);
-          if (qok) {
-            mbar_arrive_expect_tx(&sm.qfull, kQChunks * kQChunkBytes);
-            for (int c = 0; c < kQChunks; ++c)
-              tma_load_2d(sm.q[c], &map_q, &sm.qfull, 64 * c, w.r * kHq);
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, qok, 0) && warp == 4) { ok = false; break; }
-        cur_r = w.r;
-        ++sa;
-      }
-      // this tile's rows into the table (the slot read last by the previous
-      // tile's V copies is free once every producer thread is past them)
       const long long row_cur = pos_row(a, w.s, p_cur, false);
       Walker nx = w;
       nx.next(a, g);
       const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + pt) : -1;
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
-      sm.rowtab[u & 1][pt] = (int)row_cur;
+      sm.rowtab[pt] = (int)row_cur;
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
-      for (int c = 0; c < kQChunks && ok; c += 2)
-        ok = issue_pair(c, min(2, kQChunks - c), sm.rowtab[u & 1]);
-      if (ok && have_prev)
-        for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, sm.rowtab[(u - 1) & 1]);
-      have_prev = true;
+      for (int i = 0; i < kChunks && ok; ++i) {
+        const int c = chunk_at(i);
+        if (u > 0 && !warp_wait(&sm.kempty[c], (u - 1) & 1, &sm.abort)) { ok = false; break; }
+        uint8_t* base = sm.kv[c];
+#pragma unroll
+        for (int k = 0; k < kRows / 16; ++k) {
+          const int r = r0 + 16 * k;
+          const int prow = sm.rowtab[r];
+          const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + c * 128 + gq * 16 : kv;
+          cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+        pend_c[(head + npend) % kChunks] = c;
+        ++npend;
+        if (npend > 4) {
+          cp_async_wait<4>();
+          signal_oldest();
+        }
+      }
+      // the rest of this tile must land before the next tile can be waited for
+      cp_async_wait<0>();
+      while (npend > 0) signal_oldest();
       p_cur = p_next;
       w = nx;
       ++u;
     }
-    if (ok && have_prev)
-      for (int c = 0; c < kDv / 64 && ok; c += 2) ok = issue_pair(c, 2, sm.rowtab[(u - 1) & 1]);
-    flush();
+    cp_async_wait<0>();
+    while (npend > 0) signal_oldest();
     if (!ok) fail(sm, a.status);
+  } else if (warp == 9) {
+    // ----------------------------------------------------------- Q loader --
+    if (lane == 0) {
+      Walker w;
+      w.init(a, g, r_first, r_last);
+      int qs = 0;
+      bool ok = true;
+      while (w.ok && ok) {
+        for (int i = 0; i < kChunks; ++i, ++qs) {
+          const int slot = qs % kQRing;
+          if (qs >= kQRing && !mbar_wait(&sm.qempty[slot], ((qs / kQRing) - 1) & 1, &sm.abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.qfull[slot], kQChunkBytes);
+          tma_load_2d(sm.q[slot], &map_q, &sm.qfull[slot], 64 * chunk_at(i), w.r * kHq);
+        }
+        w.next(a, g);
+      }
+      if (!ok) fail(sm, a.status);
+    }
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      int slot = 0;
-      uint32_t phase = 0;
-      int u = 0, sa = 0;
+      int u = 0, sa = 0, qs = 0, cur_r = -1;
       bool ok = true;
-      struct Prev { int u, seg; bool first, last; } prev{0, 0, false, false};
-      bool have_prev = false;
-      auto consume = [&]() -> bool {
-        if (!mbar_wait(&sm.full[slot], phase, &sm.abort)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto release = [&]() {
-        mma_commit(&sm.empty[slot]);
-        if (++slot == kRing) {
-          slot = 0;
-          phase ^= 1;
-        }
-      };
-      auto do_pv = [&](const Prev& p) -> bool {
-        if (!mbar_wait(&sm.pfull, p.u & 1, &sm.abort)) return false;
-        if (p.first && p.seg > 0 && !mbar_wait(&sm.ofree, (p.seg - 1) & 1, &sm.abort)) return false;
-        tc_fence_after();
-        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
-        for (int blk = 0; blk < kDv / 128; ++blk) {
-          if (!consume()) return false;
-          const uint32_t v0 = smem_u32(sm.ring[slot]);
-          const uint32_t d = tbase + kColO + 64 * blk;
-#pragma unroll
-          for (int k = 0; k < kRows / 16; ++k) {
-            const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
-            mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
-                    (p.first && k == 0) ? 0u : 1u);
-            mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
-          }
-          release();
-        }
-        mma_commit(&sm.pempty);
-        if (p.last) mma_commit(&sm.ofull);
-        return true;
-      };
       Walker w;
       w.init(a, g, r_first, r_last);
-      int cur_r = -1;
       while (w.ok && ok) {
+        const bool first = (w.t == w.s.t0), last = (w.t == w.s.act_end - 1);
         if (w.r != cur_r) {
-          if (!mbar_wait(&sm.qfull, sa & 1, &sm.abort)) { ok = false; break; }
           cur_r = w.r;
           ++sa;
         }
         if (!mbar_wait(&sm.sempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t q0 = smem_u32(sm.q[0]);
         const uint32_t dS = tbase + kColS + 64 * (u & 1);
-        for (int c = 0; c < kQChunks && ok; c += 2) {
-          if (!consume()) { ok = false; break; }
-          const uint32_t a0 = smem_u32(sm.ring[slot]);
-          for (int i = 0; i < 2 && c + i < kQChunks; ++i) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              mma_f16(dS, smem_desc(a0 + i * kChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
-                      smem_desc(q0 + (c + i) * kQChunkBytes + 32 * k, 16, 1024, kSwizzle128B),
-                      kIdescQK, (c + i + k) > 0 ? 1u : 0u);
-            }
+        for (int i = 0; i < kChunks; ++i, ++qs) {
+          const int c = chunk_at(i), slot = qs % kQRing;
+          if (!mbar_wait(&sm.qfull[slot], (qs / kQRing) & 1, &sm.abort) ||
+              !mbar_wait(&sm.kfull[c], u & 1, &sm.abort)) {
+            ok = false;
+            break;
           }
-          release();
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sm.kv[c]), b0 = smem_u32(sm.q[slot]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(dS, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B),
+                    smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B), kIdescQK,
+                    (i + k) > 0 ? 1u : 0u);
+          mma_commit(&sm.qempty[slot]);
+          if (c == kChunks - 1) mma_commit(&sm.kempty[c]);  // QK only
         }
         if (!ok) break;
         mma_commit(&sm.sfull[u & 1]);
-        const bool first = (w.t == w.s.t0), last = (w.t == w.s.act_end - 1);
-        if (last) mma_commit(&sm.qempty);
-        if (have_prev && !do_pv(prev)) { ok = false; break; }
-        prev = Prev{u, sa - 1, first, last};
-        have_prev = true;
+        // PV of this tile once the softmax has written P^T
+        if (!mbar_wait(&sm.pfull, u & 1, &sm.abort)) { ok = false; break; }
+        if (first && sa > 1 && !mbar_wait(&sm.ofree, (sa - 2) & 1, &sm.abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        for (int blk = 0; blk < kDv / 128; ++blk) {
+          const uint32_t v0 = smem_u32(sm.kv[2 * blk]);  // chunks 2blk, 2blk+1 are 16 KB apart
+          const uint32_t d = tbase + kColO + 64 * blk;
+#pragma unroll
+          for (int k = 0; k < kRows / 16; ++k) {
+            const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
+            mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+                    (first && k == 0) ? 0u : 1u);
+            mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
+          }
+          mma_commit(&sm.kempty[2 * blk]);
+          mma_commit(&sm.kempty[2 * blk + 1]);
+        }
+        mma_commit(&sm.pempty);
+        if (last) mma_commit(&sm.ofull);
         ++u;
         w.next(a, g);
       }
-      if (ok && have_prev) ok = do_pv(prev);
       if (!ok) fail(sm, a.status);
       mma_commit(&sm.done);
       mbar_wait(&sm.done, 0, &sm.abort, 100000000ull);
@@ -511,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&sm.sempty[u & 1]);
+        if (t + 1 < s.act_end)
+          valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
         // per-head tile max
 #pragma unroll
         for (int h = 0; h < kHq; ++h) v[h] = z[h];
@@ -590,8 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.pfull);
-        if (t + 1 < s.act_end)
-          valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
         // per-head tile sum of the probabilities as the MMA sees them
 #pragma unroll
         for (int h = 0; h < kHq; ++h) v[h] = z[h];
