@@ -158,6 +158,31 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
              int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * dsa_topk_noalloc: the selection of dsa_topk (same arguments and results,
+ * minus the workspace) for callers that cannot allocate device memory: code
+ * given a stream but no allocator by the framework that owns the GPU's
+ * memory, real-time threads that must not wait on allocator locks, and
+ * deployments whose device memory is fully divided up in advance.  The pages
+ * have no counterpart; this is a deployment convenience.
+ *  Scratch: one fixed array of DSA_TOPK_NOALLOC_SCRATCH_BYTES inside the
+ *    library, present on every GPU that loads it until the process exits.  No
+ *    call allocates or frees device memory.
+ *  First call on a device: looks up the array's device address (once per
+ *    device, with that device current).  Make that first call before any
+ *    stream capture.
+ *  Limit: a problem whose scratch would exceed the array
+ *    (dsa_topk_workspace_size() > DSA_TOPK_NOALLOC_SCRATCH_BYTES) is rejected
+ *    with DSA_ERR_WORKSPACE and a message; nothing is launched.
+ *  Sharing: every call uses the same array.  Calls that overlap on the GPU
+ *    (unordered streams, several host threads) race and corrupt each other's
+ *    results; order them on one stream.  The status word is cleared at the
+ *    start of each call and cannot be read back.
+ */
+#define DSA_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
+int dsa_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
+                     int32_t* idx, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Stage 3a: sparse attention, decode (one query per sequence).
  * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
  * section 3 (3) (decode: one token per step, memory-bandwidth-bound) and the

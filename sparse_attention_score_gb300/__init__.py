@@ -84,6 +84,7 @@ _sig("dsa_index_score_prefill", _i, [_LP, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _i
                                      _vp])
 _sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
 _sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
+_sig("dsa_topk_noalloc", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
 _sig("dsa_sparse_attn_decode", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _f, _vp,
                                     _vp, _vp, _sz, _vp])
@@ -95,7 +96,7 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_index_score_workspace_size", "dsa_index_score",
            "dsa_index_score_prefill_workspace_size", "dsa_index_score_prefill",
            "dsa_topk_workspace_size",
-           "dsa_topk", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
+           "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
            "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill")
 
 
@@ -208,6 +209,20 @@ def topk(scores, n_eligible, K, idx, ws, stream=None):
     rc = _lib.dsa_topk(_ptr(scores), ld, _ptr(n_eligible), Nq, K, _ptr(idx), _ptr(ws), ws.numel(),
                        _stream(stream))
     _check(rc, "dsa_topk")
+
+
+# Size of the fixed scratch array dsa_topk_noalloc uses (DSA_TOPK_NOALLOC_SCRATCH_BYTES).
+TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def topk_noalloc(scores, n_eligible, K, idx, stream=None):
+    """dsa_topk without a workspace, for callers that may not allocate device
+    memory: the scratch is a fixed array inside the library, shared by every
+    call (calls that overlap on the GPU race)."""
+    Nq, ld = scores.shape
+    rc = _lib.dsa_topk_noalloc(_ptr(scores), ld, _ptr(n_eligible), Nq, K, _ptr(idx),
+                               _stream(stream))
+    _check(rc, "dsa_topk_noalloc")
 
 
 def sparse_attn_decode(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
