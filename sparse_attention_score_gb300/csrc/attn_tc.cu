@@ -80,7 +80,7 @@ struct __align__(1024) Smem {
   int abort;
   int rescale[2];
   float redm[4][kHq], reds[4][kHq];
-  float m_used[kHq], fscale[kHq], l_run[kHq];
+  float m_used[kHq], fscale[kHq], l_run[kHq], l_inv[kHq];
 };
 
 struct Geo {
@@ -191,15 +191,15 @@ __device__ __forceinline__ void fail(Smem& sm, int* status) {
   flag_status(status, DSA_STATUS_TIMEOUT);
 }
 
-// Transposing butterfly over a warp: on entry v[0..63] hold one value per head
-// for this lane's row; on exit v[0], v[1] hold the reduction over the 32 lanes
-// for heads hb, hb + 1, hb = 32 b4 + 16 b3 + 8 b2 + 4 b1 + 2 b0 (lane bits).
+// Transposing butterfly over a warp: on entry v[0..31] hold one value per
+// column for this lane's row; returns, in lane l, the reduction over the 32
+// lanes (rows) of column l.  31 shuffles for 32 columns.
 template <bool kMax>
-__device__ __forceinline__ void butterfly(float (&v)[kHq], int lane) {
+__device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
 #pragma unroll
   for (int st = 0; st < 5; ++st) {
     const int o = 16 >> st;
-    const int n = kHq >> st;  // live values
+    const int n = 32 >> st;  // live values
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < n / 2; ++i) {
@@ -209,11 +209,7 @@ __device__ __forceinline__ void butterfly(float (&v)[kHq], int lane) {
       v[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-}
-
-__device__ __forceinline__ int butterfly_head(int lane) {
-  return 32 * ((lane >> 4) & 1) + 16 * ((lane >> 3) & 1) + 8 * ((lane >> 2) & 1) +
-         4 * ((lane >> 1) & 1) + 2 * (lane & 1);
+  return v[0];
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -286,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x < kHq) {
     sm.m_used[threadIdx.x] = -INFINITY;
     sm.l_run[threadIdx.x] = 0.0f;
+    sm.fscale[threadIdx.x] = 1.0f;
   }
   if (warp == 8) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -310,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const char* kv = reinterpret_cast<const char*>(a.kp);
     uint32_t ps = 0;
     bool ok = true;
-    int pend_c[kChunks];
-    int npend = 0, head = 0;
+    // Chunks of a tile are issued in chunk_at order and all signalled before
+    // the next tile starts, so two counters name the oldest unsignalled one.
+    int issued = 0, sig = 0;
     auto signal_oldest = [&]() {
       fence_proxy_async_smem();
-      mbar_arrive(&sm.kfull[pend_c[head]]);
-      head = (head + 1) % kChunks;
-      --npend;
+      mbar_arrive(&sm.kfull[chunk_at(sig)]);
+      ++sig;
     };
     Walker w;
     w.init(a, g, r_first, r_last);
@@ -342,22 +339,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
         }
         cp_async_commit();
-        pend_c[(head + npend) % kChunks] = c;
-        ++npend;
-        if (npend > 4) {
+        if (++issued - sig > 4) {
           cp_async_wait<4>();
           signal_oldest();
         }
       }
       // the rest of this tile must land before the next tile can be waited for
       cp_async_wait<0>();
-      while (npend > 0) signal_oldest();
+      while (sig < issued) signal_oldest();
+      issued = sig = 0;
       p_cur = p_next;
       w = nx;
       ++u;
     }
     cp_async_wait<0>();
-    while (npend > 0) signal_oldest();
+    while (sig < issued) signal_oldest();
     if (!ok) fail(sm, a.status);
   } else if (warp == 9) {
     // ----------------------------------------------------------- Q loader --
@@ -444,8 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax + finalize --
-    const int row = threadIdx.x;  // TMEM lane = row of the tile = dv lane of O
-    const int hb = butterfly_head(lane);
+    // Thread = TMEM lane = row of the tile (and dv lane of O at the end).
+    // The loops over 32-column groups stay rolled: this code runs once per
+    // tile, so it has to stay small enough to be fetched quickly.
+    const int row = threadIdx.x;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float c = a.scale_log2;
     int u = 0, sa = 0;
     uint32_t sp = 0;
@@ -468,145 +467,139 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // validity of this thread's row is looked up one tile ahead
       bool valid_next = pos_row(a, s, sel_pos(a, s, (long long)s.t0 * kRows + row), true) >= 0;
+      bool pend_l = false;  // reds hold a tile's sums not yet added to l_run
       for (int t = s.t0; t < s.act_end; ++t) {
         const bool valid = valid_next;
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
-        float z[kHq], v[kHq];
-        {
+        const uint32_t ta = tbase + lanes + kColS + 64 * (u & 1);
+        // pass 1: per-head maximum of the tile
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
           uint32_t raw[32];
-          const uint32_t ta = tbase + ((uint32_t)(warp * 32) << 16) + kColS + 64 * (u & 1);
-          tmem_ld_32cols(ta, raw);
+          tmem_ld_32cols(ta + 32 * half, raw);
           tmem_wait_ld();
+          float v[32];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) z[h] = valid ? __uint_as_float(raw[h]) * c : -INFINITY;
-          tmem_ld_32cols(ta + 32, raw);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) z[32 + h] = valid ? __uint_as_float(raw[h]) * c : -INFINITY;
+          for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
+          sm.redm[warp][32 * half + lane] = butterfly32<true>(v, lane);
         }
-        tc_fence_before();
-        mbar_arrive(&sm.sempty[u & 1]);
         if (t + 1 < s.act_end)
           valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
-        // per-head tile max
-#pragma unroll
-        for (int h = 0; h < kHq; ++h) v[h] = z[h];
-        butterfly<true>(v, lane);
-        sm.redm[warp][hb] = v[0];
-        sm.redm[warp][hb + 1] = v[1];
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        if (warp == 0) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = hb + e;
-            const float mt = fmaxf(fmaxf(sm.redm[0][h], sm.redm[1][h]),
-                                   fmaxf(sm.redm[2][h], sm.redm[3][h]));
-            const float mo = sm.m_used[h];
-            float mn = mo, f = 1.0f;
-            if (mt > mo + kRescaleLog2 || (mo == -INFINITY && mt > -INFINITY)) {
-              mn = mt;
-              if (mo > -INFINITY) {
-                f = exp2f(mo - mn);
-                sm.rescale[u & 1] = 1;
-              }
+        if (row < kHq) {
+          // thread h owns head h: the previous tile's sums, then the new max
+          const int h = row;
+          if (pend_l)
+            sm.l_run[h] = sm.l_run[h] * sm.fscale[h] +
+                          ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
+          const float mt = fmaxf(fmaxf(sm.redm[0][h], sm.redm[1][h]),
+                                 fmaxf(sm.redm[2][h], sm.redm[3][h]));
+          const float mo = sm.m_used[h];
+          float mn = mo, f = 1.0f;
+          if (mt > mo + kRescaleLog2 || (mo == -INFINITY && mt > -INFINITY)) {
+            mn = mt;
+            if (mo > -INFINITY) {
+              f = exp2f(mo - mn);
+              sm.rescale[u & 1] = 1;
             }
-            sm.m_used[h] = mn;
-            sm.fscale[h] = f;
           }
+          sm.m_used[h] = mn;
+          sm.fscale[h] = f;
         }
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
         const bool resc = sm.rescale[u & 1] != 0;
-        if (threadIdx.x == 0) sm.rescale[(u + 1) & 1] = 0;
-        // P = 2^(z - m), kept as the exact fp32 sum of its bf16 hi and lo parts
-        // (the values the two PV MMAs multiply); the row sums use the same.
-#pragma unroll
-        for (int h = 0; h < kHq; ++h) {
-          const float mu = sm.m_used[h];
-          const float pf = (mu == -INFINITY) ? 0.0f : exp2f(z[h] - mu);
-          const float hi = __bfloat162float(__float2bfloat16_rn(pf));
-          z[h] = hi + __bfloat162float(__float2bfloat16_rn(pf - hi));
-        }
+        if (row == 0) sm.rescale[(u + 1) & 1] = 0;
         // the previous PV must be done before P^T (and, if needed, O) change
         if (!warp_wait(&sm.pempty, (u & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         if (resc) {
-          for (int blk = 0; blk < kDv / 128; ++blk) {
-            for (int half = 0; half < 2; ++half) {
-              uint32_t raw[32];
-              const uint32_t ta = tbase + ((uint32_t)(warp * 32) << 16) + kColO + 64 * blk + 32 * half;
-              tmem_ld_32cols(ta, raw);
-              tmem_wait_ld();
+#pragma unroll 1
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t to = tbase + lanes + kColO + 64 * (q >> 1) + 32 * (q & 1);
+            uint32_t raw[32];
+            tmem_ld_32cols(to, raw);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                raw[i] = __float_as_uint(__uint_as_float(raw[i]) * sm.fscale[32 * half + i]);
-              tmem_st_32cols(ta, raw);
-            }
+            for (int i = 0; i < 32; ++i)
+              raw[i] = __float_as_uint(__uint_as_float(raw[i]) * sm.fscale[32 * (q & 1) + i]);
+            tmem_st_32cols(to, raw);
           }
           tmem_wait_st();
         }
-        {
-          uint8_t* rh = sm.phi + row * 128;
-          uint8_t* rl = sm.plo + row * 128;
+        // pass 2: P = 2^(z - m) as bf16 hi + lo into this row of P^T; the
+        // per-head sums add exactly the values the two PV MMAs multiply
+        uint8_t* rh = sm.phi + row * 128;
+        uint8_t* rl = sm.plo + row * 128;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t raw[32];
+          tmem_ld_32cols(ta + 32 * half, raw);
+          tmem_wait_ld();
+          float v[32];
+          uint32_t hw[16], lw[16];
 #pragma unroll
-          for (int gq = 0; gq < 8; ++gq) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float a0 = z[8 * gq + 2 * k], a1 = z[8 * gq + 2 * k + 1];
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
-              const float2 hf = __bfloat1622float2(hi);
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-              hw[k] = *reinterpret_cast<const uint32_t*>(&hi);
-              lw[k] = *reinterpret_cast<const uint32_t*>(&lo);
-            }
-            const int off = (gq ^ (row & 7)) << 4;
-            *reinterpret_cast<uint4*>(rh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(rl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int i = 0; i < 32; i += 2) {
+            // branch-free: an unusable row gives 2^-inf = 0 (a usable row makes
+            // every head's running max finite)
+            const float m0 = sm.m_used[32 * half + i], m1 = sm.m_used[32 * half + i + 1];
+            const float p0 = ex2_approx(valid ? __uint_as_float(raw[i]) * c - m0 : -INFINITY);
+            const float p1 = ex2_approx(valid ? __uint_as_float(raw[i + 1]) * c - m1 : -INFINITY);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+            const float2 lf = __bfloat1622float2(lo);
+            v[i] = hf.x + lf.x;
+            v[i + 1] = hf.y + lf.y;
+            hw[i / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+            lw[i / 2] = *reinterpret_cast<const uint32_t*>(&lo);
           }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int off = ((4 * half + k) ^ (row & 7)) << 4;
+            *reinterpret_cast<uint4*>(rh + off) =
+                make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+            *reinterpret_cast<uint4*>(rl + off) =
+                make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          }
+          sm.reds[warp][32 * half + lane] = butterfly32<false>(v, lane);
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        mbar_arrive(&sm.sempty[u & 1]);
         mbar_arrive(&sm.pfull);
-        // per-head tile sum of the probabilities as the MMA sees them
-#pragma unroll
-        for (int h = 0; h < kHq; ++h) v[h] = z[h];
-        butterfly<false>(v, lane);
-        sm.reds[warp][hb] = v[0];
-        sm.reds[warp][hb + 1] = v[1];
-        if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        if (warp == 0) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = hb + e;
-            sm.l_run[h] = sm.l_run[h] * sm.fscale[h] +
-                          ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
-          }
-        }
+        pend_l = true;
         ++u;
       }
       if (!ok) break;
       // ---- finalize the query segment: O out of TMEM ----
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // last tile's sums
+      if (row < kHq) {
+        const int h = row;
+        const float l = sm.l_run[h] * sm.fscale[h] +
+                        ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
+        sm.l_run[h] = l;
+        sm.l_inv[h] = l > 0.0f ? 1.0f / l : 0.0f;
+      }
       if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // l_run final
       if (!warp_wait(&sm.ofull, sa & 1, &sm.abort)) { ok = false; break; }
       tc_fence_after();
-      for (int blk = 0; blk < kDv / 128; ++blk) {
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        const int blk = q >> 1, half = q & 1;
+        uint32_t raw[32];
+        tmem_ld_32cols(tbase + lanes + kColO + 64 * blk + 32 * half, raw);
+        tmem_wait_ld();
         const int dv = blk * 128 + row;
-        for (int half = 0; half < 2; ++half) {
-          uint32_t raw[32];
-          tmem_ld_32cols(tbase + ((uint32_t)(warp * 32) << 16) + kColO + 64 * blk + 32 * half, raw);
-          tmem_wait_ld();
+        if (s.complete) {
+          __nv_bfloat16* o = out + (size_t)(32 * half) * kDv + dv;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = 32 * half + i;
-            const float o = __uint_as_float(raw[i]);
-            if (s.complete) {
-              const float l = sm.l_run[h];
-              out[(size_t)h * kDv + dv] = __float2bfloat16(l > 0.0f ? o / l : 0.0f);
-            } else {
-              po[(size_t)h * kDv + dv] = o;
-            }
-          }
+          for (int i = 0; i < 32; ++i)
+            o[(size_t)i * kDv] = __float2bfloat16(__uint_as_float(raw[i]) * sm.l_inv[32 * half + i]);
+        } else {
+          float* o = po + (size_t)(32 * half) * kDv + dv;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[(size_t)i * kDv] = __uint_as_float(raw[i]);
         }
       }
       if (row < kHq) {
@@ -626,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row < kHq) {
         sm.m_used[row] = -INFINITY;
         sm.l_run[row] = 0.0f;
+        sm.fscale[row] = 1.0f;
       }
       ++sa;
       ok = ok && !sm.abort;
@@ -656,26 +650,37 @@ __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, cons
   if (g.lo_of(c - 1) > first) return;  // an earlier boundary of this query merges it
   const int c0 = g.cta_of(first), c1 = g.cta_of(first + g.Tq - 1);
   const int h0 = blockIdx.x * 8;
-  __shared__ float wgt[8][kMaxCtas + 1];
+  __shared__ float wgt[8][kMaxCtas + 1], lpart[8][kMaxCtas + 1];
   __shared__ float lsum[8], mmax[8];
-  if (threadIdx.x < 8) {
-    const int h = h0 + threadIdx.x;
+  const int ns = c1 - c0 + 1;
+  // (m, l) of every slot and head of this group, loaded all at once
+  for (int i = threadIdx.x; i < ns * 8; i += blockDim.x) {
+    const int cc = c0 + i / 8, hh = i % 8;
+    const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+    const float2 ml =
+        __ldcg(reinterpret_cast<const float2*>(part_ml + ((size_t)ps * kHq + h0 + hh) * 2));
+    wgt[hh][i / 8] = ml.y > 0.0f ? ml.x : -INFINITY;
+    lpart[hh][i / 8] = ml.y;
+  }
+  __syncthreads();
+  {
+    // warp hh: M = max m_s, weights 2^(m_s - M), L = sum l_s 2^(m_s - M)
+    const int hh = threadIdx.x >> 5, ln = threadIdx.x & 31;
     float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) {
-      const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-      const float l = part_ml[((size_t)ps * kHq + h) * 2 + 1];
-      if (l > 0.0f) M = fmaxf(M, part_ml[((size_t)ps * kHq + h) * 2]);
-    }
+    for (int j = ln; j < ns; j += 32) M = fmaxf(M, wgt[hh][j]);
+    M = warp_max(M);
     float L = 0.0f;
-    for (int cc = c0; cc <= c1; ++cc) {
-      const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-      const float l = part_ml[((size_t)ps * kHq + h) * 2 + 1];
-      const float w = l > 0.0f ? exp2f(part_ml[((size_t)ps * kHq + h) * 2] - M) : 0.0f;
-      wgt[threadIdx.x][cc - c0] = w;
-      L += l * w;
+    for (int j = ln; j < ns; j += 32) {
+      const float mj = wgt[hh][j];
+      const float w = mj > -INFINITY ? exp2f(mj - M) : 0.0f;
+      L += lpart[hh][j] * w;
+      wgt[hh][j] = w;
     }
-    lsum[threadIdx.x] = L;
-    mmax[threadIdx.x] = M;
+    L = warp_sum(L);
+    if (ln == 0) {
+      lsum[hh] = L;
+      mmax[hh] = M;
+    }
   }
   __syncthreads();
   // thread t owns outputs t + 256 k (k < 16): head k/2, dv t + 256 (k & 1);

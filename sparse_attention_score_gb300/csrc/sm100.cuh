@@ -22,6 +22,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32): a single
+// instruction without branches, accurate to a few fp32 ulp; results below
+// 2^-126 flush to zero and 2^-inf = 0.  For values that are rounded to bf16
+// right after, where this error does not show.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
