@@ -56,21 +56,83 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    """SM clock and clock-event reasons of one GPU, sampled while the timed
+    region runs.  Reads NVML directly (read-only queries, as fast as the host
+    thread can poll, so even a region of a few milliseconds gets samples);
+    falls back to `nvidia-smi -lms 100` when NVML cannot be loaded."""
 
+    # nvmlClocksEventReason* bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []          # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
         self.proc = None
         self.lines = []
+        self.nvml = None
+        self.handle = None
+        self._stop = threading.Event()
+        self.t = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = 1
+            bus = self._pci_bus_id()
+            if bus:
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h))
+            if rc != 0:
+                return
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self.nvml, self.handle, self.ct = nv, h, ctypes
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _pci_bus_id(self):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(self.cuda_index)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return None
+
+    def _poll(self):
+        ct, nv, h = self.ct, self.nvml, self.handle
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0 and \
+                    self.reason_fn(h, ct.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(0.0002)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
 
     def start(self):
+        if self.nvml is not None:
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 1.0:
+                time.sleep(0.0005)
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                ["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
@@ -78,11 +140,16 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
+        if self.nvml is not None:
+            self._stop.set()
+            self.t.join(timeout=2)
+            if not self.samples:
+                return None
+            reasons = sorted({nm for _, r in self.samples for b, nm in self.REASONS.items() if r & b})
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                    "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                    "samples": len(self.samples), "source": "nvml"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -108,7 +175,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 def kernel_source_sha(names):
@@ -329,8 +396,8 @@ def roofline_of(res, peaks):
     st = res["stage_ms"]  # [index, topk, attn] ms per step (avg)
     if case.kind == "decode":
         cands = {
-            "index_score": (alg["index_bytes"], st[0], ["index_score.cu"]),
-            "sparse_attn": (alg["gather_bytes"], st[2], ["attn.cu"]),
+            "index_score": (alg["index_bytes"], st[0], ["index_score.cu", "index_tc.cu"]),
+            "sparse_attn": (alg["gather_bytes"], st[2], ["attn.cu", "attn_tc.cu"]),
         }
         dom = max(cands, key=lambda k: cands[k][1])
         nbytes, ms, srcs = cands[dom]
@@ -342,8 +409,8 @@ def roofline_of(res, peaks):
         step_bytes = alg["index_bytes"] + alg["gather_bytes"]
         return roof, step_bytes
     cands = {
-        "index_score": (alg["index_flops"], st[0], ["index_score.cu"]),
-        "sparse_attn": (alg["attn_flops"], st[2], ["attn.cu"]),
+        "index_score": (alg["index_flops"], st[0], ["index_score.cu", "index_prefill_tc.cu"]),
+        "sparse_attn": (alg["attn_flops"], st[2], ["attn.cu", "attn_tc.cu"]),
     }
     dom = max(cands, key=lambda k: cands[k][1])
     fl, ms, srcs = cands[dom]

@@ -66,32 +66,28 @@ __device__ __forceinline__ int block_incl_scan(int v, int* sh) {
   return r;
 }
 
-// One radix pass over the keys matching (prefix, mask): histogram of the
-// `bits`-wide digit at `shift`, then the digit that holds the remaining-th
-// largest key.  Updates prefix/mask/remaining.
+// One radix digit: histogram of the `bits`-wide digit at `shift` over the keys
+// matching (prefix, mask), then the digit holding the remaining-th largest
+// key.  Updates prefix/mask/remaining.  Keys are read four at a time; the
+// digits below the bits shared by every key of the block are diverse enough
+// that plain shared atomics rarely collide.
 __device__ __forceinline__ void radix_pass(const uint32_t* keys, int cnt, int shift, int bits,
                                            uint32_t& prefix, uint32_t& mask, int& remaining,
                                            Shared& sh) {
   const int nb = 1 << bits;
   for (int i = threadIdx.x; i < nb; i += kThreads) sh.hist[i] = 0;
   __syncthreads();
-  // Scores concentrate in a few digits (integer scores share an exponent), so
-  // equal bins of a warp are combined first: one shared atomic per distinct bin.
-  const int lane = threadIdx.x & 31;
-  for (int base = 0; base < cnt; base += kThreads) {
-    const int i = base + threadIdx.x;
-    uint32_t k = 0;
-    bool m = false;
-    if (i < cnt) {
-      k = keys[i];
-      m = (k & mask) == prefix;
-    }
-    const unsigned active = __ballot_sync(0xffffffffu, m);
-    if (m) {
-      const uint32_t bin = (k >> shift) & (uint32_t)(nb - 1);
-      const unsigned peers = __match_any_sync(active, bin);
-      if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], __popc(peers));
-    }
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int n4 = (cnt + 3) >> 2;  // the array has room for three keys past cnt
+  const uint32_t dm = (uint32_t)(nb - 1);
+#pragma unroll 4
+  for (int j = threadIdx.x; j < n4; j += kThreads) {
+    const uint4 v = k4[j];
+    const int i0 = 4 * j;
+    if ((v.x & mask) == prefix) atomicAdd(&sh.hist[(v.x >> shift) & dm], 1);
+    if (i0 + 1 < cnt && (v.y & mask) == prefix) atomicAdd(&sh.hist[(v.y >> shift) & dm], 1);
+    if (i0 + 2 < cnt && (v.z & mask) == prefix) atomicAdd(&sh.hist[(v.z >> shift) & dm], 1);
+    if (i0 + 3 < cnt && (v.w & mask) == prefix) atomicAdd(&sh.hist[(v.w >> shift) & dm], 1);
   }
   __syncthreads();
   // thread t owns bins nb-1-2t and nb-2-2t (highest digits first)
@@ -112,43 +108,80 @@ __device__ __forceinline__ void radix_pass(const uint32_t* keys, int cnt, int sh
   __syncthreads();
   remaining -= sh.sel_above;
   prefix |= (uint32_t)sh.sel_bin << shift;
-  mask |= (uint32_t)(nb - 1) << shift;
+  mask |= dm << shift;
   __syncthreads();
 }
 
-struct Job {
-  const float* scores;  // block mode: row base
-  long long start;      // block mode: first position of the block
-  int cnt;              // keys in this CTA
-  int K;                // keys to keep
-  int32_t* out_pos;     // destination of kept positions (ascending)
-  uint32_t* out_key;    // block mode with merge pending: kept keys too
-  const int32_t* cand_pos;  // merge mode: positions of the loaded keys (chunked)
-};
+// Minimum and maximum key over the block (every thread gets both).
+__device__ __forceinline__ void block_min_max(uint32_t& lo, uint32_t& hi, Shared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    sh.wgt[warp] = (int)lo;
+    sh.weq[warp] = (int)hi;
+  }
+  __syncthreads();
+  lo = __reduce_min_sync(0xffffffffu, (uint32_t)sh.wgt[lane]);
+  hi = __reduce_max_sync(0xffffffffu, (uint32_t)sh.weq[lane]);
+  __syncthreads();
+}
 
-// Emit the kept positions in ascending order.  pos_of(i) maps a key index to
-// its position.
+// Exact K-th largest key: the bits shared by every key (from the block's
+// minimum and maximum) are fixed at once, the rest in digits of up to 11 bits.
+// On return `prefix` is the threshold key T and `remaining` the number of keys
+// equal to T to keep.
+__device__ __forceinline__ void select_threshold(const uint32_t* keys, int cnt, uint32_t kmin,
+                                                 uint32_t kmax, uint32_t& prefix, int& remaining,
+                                                 Shared& sh) {
+  uint32_t mask = 0;
+  prefix = 0;
+  if (kmin == kmax) {
+    prefix = kmax;  // every key ties: T is that key
+    return;
+  }
+  const int hb = 31 - __clz(kmin ^ kmax);  // highest bit where keys differ
+  mask = hb == 31 ? 0u : ~((2u << hb) - 1u);
+  prefix = kmax & mask;
+  int hi = hb;
+  while (hi >= 0) {
+    const int bits = hi + 1 < 11 ? hi + 1 : 11;
+    const int shift = hi + 1 - bits;
+    radix_pass(keys, cnt, shift, bits, prefix, mask, remaining, sh);
+    hi = shift - 1;
+  }
+}
+
+// Emit the kept positions in ascending order: every key > T and the first
+// `need` keys == T (position order).  pos_of(i) maps a key index to its
+// position.  Each warp takes a contiguous segment (a multiple of 128 keys);
+// per step a lane holds four consecutive keys and one warp scan of packed
+// (greater, equal) counts places them.
 template <typename PosOf>
 __device__ __forceinline__ void emit(const uint32_t* keys, int cnt, uint32_t T, int need,
                                      bool take_all, int32_t* out_pos, uint32_t* out_key,
                                      PosOf pos_of, Shared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = ((cnt + kThreads - 1) / kThreads) * 32;
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int seg = ((cnt + kThreads * 4 - 1) / (kThreads * 4)) * 128;
   const int s0 = warp * seg, s1 = min(cnt, s0 + seg);
   int gt = 0, eq = 0;
-  if (!take_all) {
-    for (int i = s0 + lane; i < s1; i += 32) {
-      const uint32_t k = keys[i];
-      gt += k > T;
-      eq += k == T;
-    }
+  for (int base = s0; base < s1; base += 128) {
+    const int i0 = base + 4 * lane;
+    const uint4 v = i0 < s1 ? k4[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o);
-      eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    for (int e = 0; e < 4; ++e) {
+      if (i0 + e < s1) {
+        gt += take_all || kv[e] > T;
+        eq += !take_all && kv[e] == T;
+      }
     }
-  } else {
-    gt = max(0, s1 - s0);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
   }
   if (lane == 0) {
     sh.wgt[warp] = gt;
@@ -171,30 +204,45 @@ __device__ __forceinline__ void emit(const uint32_t* keys, int cnt, uint32_t T, 
     sh.weq[lane] = ei - e;
   }
   __syncthreads();
-  const int eq_off = sh.weq[warp];
-  const int quota = take_all ? 0 : max(0, min(eq, need - eq_off));
-  int w = sh.wgt[warp] + (take_all ? 0 : min(eq_off, need));
-  int eq_seen = 0;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int base = s0; base < s1; base += 32) {
-    const int i = base + lane;
-    bool keep = false, is_eq = false;
-    uint32_t k = 0;
-    if (i < s1) {
-      k = keys[i];
-      keep = take_all || k > T;
-      is_eq = !take_all && k == T;
+  int eq_seen = sh.weq[warp];  // keys == T before this step, in position order
+  int w = sh.wgt[warp] + max(0, min(eq_seen, need));
+  for (int base = s0; base < s1; base += 128) {
+    const int i0 = base + 4 * lane;
+    const uint4 v = i0 < s1 ? k4[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+    int cg = 0, cq = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i0 + e < s1) {
+        cg += take_all || kv[e] > T;
+        cq += !take_all && kv[e] == T;
+      }
     }
-    const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
-    if (is_eq && eq_seen + __popc(eqb & lt) < quota) keep = true;
-    eq_seen += __popc(eqb);
-    const unsigned kb = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int o = w + __popc(kb & lt);
-      out_pos[o] = pos_of(i);
-      if (out_key) out_key[o] = k;
+    const int packed = cg | (cq << 16);
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
     }
-    w += __popc(kb);
+    const int excl = incl - packed;
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    int eqr = eq_seen + (excl >> 16);  // rank among keys == T of this lane's first one
+    int o = w + (excl & 0xFFFF) + max(0, min(excl >> 16, need - eq_seen));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i0 + e < s1) {
+        bool keep = take_all || kv[e] > T;
+        if (!take_all && kv[e] == T) keep = eqr++ < need;
+        if (keep) {
+          out_pos[o] = pos_of(i0 + e);
+          if (out_key) out_key[o] = kv[e];
+          ++o;
+        }
+      }
+    }
+    w += (tot & 0xFFFF) + max(0, min(tot >> 16, need - eq_seen));
+    eq_seen += tot >> 16;
   }
 }
 
@@ -202,9 +250,10 @@ __device__ __forceinline__ void emit(const uint32_t* keys, int cnt, uint32_t T, 
 // mode 1: block step writing the block's winners to the workspace
 // mode 2: merge step over a row's block winners
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_topk_block(TopkParams a, int nchunks, uint32_t* cand_key, int32_t* cand_pos, int* cand_cnt) {
-  extern __shared__ uint32_t keys[];
+  extern __shared__ uint4 keys_raw[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(keys_raw);
   __shared__ Shared sh;
   grid_dependency_wait();
   launch_dependents();
@@ -219,12 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int K = a.K;
   int cnt;
   long long start = 0;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   if (kMode != 2) {
     start = (long long)c * kCap;
     const long long rem = n - start;
     cnt = (int)(rem < 0 ? 0 : (rem > kCap ? kCap : rem));
     const float* src = a.scores + (long long)r * a.ld + start;
-    for (int i = threadIdx.x; i < cnt; i += kThreads) keys[i] = score_key(__ldg(&src[i]));
+#pragma unroll 8
+    for (int i = threadIdx.x; i < cnt; i += kThreads) {
+      const uint32_t k = score_key(__ldg(&src[i]));
+      keys[i] = k;
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
   } else {
     if (threadIdx.x == 0) {
       int off = 0;
@@ -239,35 +295,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nchunks; ++j) {
       const int o = sh.chunk_off[j], m = sh.chunk_off[j + 1] - o;
       const uint32_t* src = cand_key + ((long long)r * nchunks + j) * K;
-      for (int i = threadIdx.x; i < m; i += kThreads) keys[o + i] = __ldg(&src[i]);
+#pragma unroll 4
+      for (int i = threadIdx.x; i < m; i += kThreads) {
+        const uint32_t k = __ldg(&src[i]);
+        keys[o + i] = k;
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
     }
   }
-  __syncthreads();
+  block_min_max(kmin, kmax, sh);  // includes the barrier after the loads
 
   const int keep_n = cnt < K ? cnt : K;
   const bool take_all = keep_n == cnt;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = keep_n;
-  if (!take_all) {
-    radix_pass(keys, cnt, 21, 11, prefix, mask, remaining, sh);
-    radix_pass(keys, cnt, 10, 11, prefix, mask, remaining, sh);
-    radix_pass(keys, cnt, 0, 10, prefix, mask, remaining, sh);
-  }
+  uint32_t T = 0;
+  int need = keep_n;
+  if (!take_all) select_threshold(keys, cnt, kmin, kmax, T, need, sh);
 
   if (kMode == 0) {
     int32_t* out = a.idx + (long long)r * K;
-    emit(keys, cnt, prefix, remaining, take_all, out, (uint32_t*)nullptr,
+    emit(keys, cnt, T, need, take_all, out, (uint32_t*)nullptr,
          [&](int i) { return (int32_t)(start + i); }, sh);
     for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
   } else if (kMode == 1) {
     const long long slot = (long long)r * nchunks + c;
-    emit(keys, cnt, prefix, remaining, take_all, cand_pos + slot * K, cand_key + slot * K,
+    emit(keys, cnt, T, need, take_all, cand_pos + slot * K, cand_key + slot * K,
          [&](int i) { return (int32_t)(start + i); }, sh);
     if (threadIdx.x == 0) cand_cnt[slot] = keep_n;
   } else {
     int32_t* out = a.idx + (long long)r * K;
     const int32_t* cp = cand_pos + (long long)r * nchunks * K;
-    emit(keys, cnt, prefix, remaining, take_all, out, (uint32_t*)nullptr,
+    emit(keys, cnt, T, need, take_all, out, (uint32_t*)nullptr,
          [&](int i) {
            int j = 0;
            while (j + 1 < nchunks && sh.chunk_off[j + 1] <= i) ++j;
@@ -283,7 +341,7 @@ void set_smem_attr() {
   static bool done = false;
   if (!done) {
     cudaFuncSetAttribute(k_topk_block<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kCap * (int)sizeof(uint32_t));
+                         (kCap + 4) * (int)sizeof(uint32_t));
     done = true;
   }
 }
@@ -305,10 +363,13 @@ size_t topk_smem_ws(int Nq, long long ld, int K) {
 
 int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   const int nch = topk_chunks(p.ld);
-  const size_t smem = kCap * sizeof(uint32_t);
+  const size_t smem = (kCap + 4) * sizeof(uint32_t);
   if (nch == 1) {
+    // a row shorter than the cap needs only its own keys in shared memory,
+    // so that two CTAs (two rows) share an SM
     set_smem_attr<0>();
-    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem, s, p, 1,
+    const size_t smem0 = (size_t)((p.ld + 4 + 3) & ~3LL) * sizeof(uint32_t);
+    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem0, s, p, 1,
                                      (uint32_t*)nullptr, (int32_t*)nullptr, (int*)nullptr);
     count_launch();
     if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));

@@ -263,6 +263,30 @@ def test_topk_long_rows_ties_across_blocks(K):
     assert dsa.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("ld,K", [(20000, 2048), (65536, 4096), (4097, 7)])
+def test_topk_single_block_rows_ties_and_edges(ld, K):
+    """Rows of 4K..64K positions (one shared-memory block each): heavy ties,
+    empty, short and exact-K rows, one value everywhere, -0 against +0, and
+    winners only at the end of the row."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(ld + K)
+    Nq = 9
+    s = rng.integers(0, 4, size=(Nq, ld)).astype(np.float32)
+    s[1] = rng.standard_normal(ld).astype(np.float32)
+    s[2, :] = 5.0
+    s[3, ld - ld // 9:] = 9.0
+    s[4, ::3] = -0.0
+    n = np.array([ld, ld - 1, ld // 2, ld, 4096, 0, 1, K, K + 1], np.int32)
+    st, ne = torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda()
+    idx = torch.empty((Nq, K), dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(dsa.topk_workspace_size(Nq, ld, K))
+    dsa.topk(st, ne, K, idx, ws)
+    got = idx.cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.topk(s, n, K))
+    assert dsa.get_status(ws) == 0
+
+
 def test_prefill_indexer_both_entry_points():
     """The prefill form (queries of one sequence sharing key tiles) and the
     general form (explicit q_seq) give the oracle's scores bit for bit."""
