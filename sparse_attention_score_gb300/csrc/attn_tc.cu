@@ -53,7 +53,7 @@ constexpr int kHq = 64, kDqk = 576, kDv = 512;
 constexpr int kRows = 128;
 constexpr int kChunks = kDqk / 64;           // 9 K chunks of 64 dims; the first 8 are V
 constexpr int kChunkBytes = kRows * 128;     // 64 dims x 128 rows, bf16
-constexpr int kQRing = 3;                    // Q chunks in flight
+constexpr int kQRing = 5;                    // Q chunks in flight
 constexpr int kQChunkBytes = kHq * 128;      // 8 KB
 constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
 constexpr int kThreads = 320;                // 4 softmax + 4 producer + MMA + Q loader warps
@@ -233,6 +233,14 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// One arrival on `bar` once every cp.async this thread has issued so far has
+// landed; the thread does not wait (the arrival counts toward the barrier's
+// expected count).  The consumer makes the data visible to the tensor cores
+// with a proxy fence after its wait.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -300,21 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each 128-byte row chunk is copied by 8 consecutive threads (16 B each),
     // so a warp instruction moves four whole rows; thread t copies granule
     // t % 8 of rows t / 8 + 16 i.  The tile's physical rows are looked up
-    // once (thread t: row t) into a shared table.  Up to four chunks are in
-    // flight per thread before the oldest is waited for and signalled.
+    // once (thread t: row t) into a shared table.  A chunk's full barrier
+    // is armed by the copies themselves, so the producer never waits for
+    // its own loads: every slot is refilled as soon as it is released.
     const int pt = threadIdx.x - 128;
     const int gq = pt & 7, r0 = pt >> 3;
     const char* kv = reinterpret_cast<const char*>(a.kp);
     uint32_t ps = 0;
     bool ok = true;
-    // Chunks of a tile are issued in chunk_at order and all signalled before
-    // the next tile starts, so two counters name the oldest unsignalled one.
-    int issued = 0, sig = 0;
-    auto signal_oldest = [&]() {
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.kfull[chunk_at(sig)]);
-      ++sig;
-    };
     Walker w;
     w.init(a, g, r_first, r_last);
     int u = 0;
@@ -338,22 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + c * 128 + gq * 16 : kv;
           cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
         }
-        cp_async_commit();
-        if (++issued - sig > 4) {
-          cp_async_wait<4>();
-          signal_oldest();
-        }
+        cp_async_arrive(&sm.kfull[c]);
       }
-      // the rest of this tile must land before the next tile can be waited for
-      cp_async_wait<0>();
-      while (sig < issued) signal_oldest();
-      issued = sig = 0;
       p_cur = p_next;
       w = nx;
       ++u;
     }
     cp_async_wait<0>();
-    while (sig < issued) signal_oldest();
     if (!ok) fail(sm, a.status);
   } else if (warp == 9) {
     // ----------------------------------------------------------- Q loader --
@@ -399,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          fence_proxy_async_smem();  // the copies' writes, seen by the tensor cores
           tc_fence_after();
           const uint32_t a0 = smem_u32(sm.kv[c]), b0 = smem_u32(sm.q[slot]);
 #pragma unroll
