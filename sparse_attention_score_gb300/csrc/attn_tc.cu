@@ -7,38 +7,35 @@
 // every query attends, exactly, over its own selected rows only, gathered from
 // the paged cache through the block table.
 //
-// Work unit: a tile of 64 selected rows of one query.  Per tile:
-//   QK  S[128 x 64 rows] = Q[128 x 576] . K_rows[64 x 576]^T    (TMEM, fp32)
-//       A = the query's 64 heads as M rows 0-63 (a Q chunk from the ring;
-//       M rows 64-127 read whatever follows in shared memory and land in TMEM
-//       lanes nobody reads), B = the gathered rows; both K-major in 9 chunks
-//       of 64 dims (128-byte swizzle); 36 tcgen05.mma kind::f16 (K = 16).
-//       One TMEM lane holds one head, so the softmax is thread-local: thread
-//       h keeps head h's running max m (raised only when a tile exceeds it by
-//       more than 2^8; O is rescaled in TMEM then) and running sum l.
-//       P = 2^(z - m) is split into bf16 hi + lo and l sums hi + lo exactly,
-//       so the only rounding left in the output is its final bf16 store.
-//   PV  O^T[512 dv x 64 heads] += V^T[512 x 64 rows] . P^T[64 rows x 64]
+// Work unit: a tile of 128 selected rows of one query.  Per tile:
+//   QK  S^T[128 rows x 64 heads] = K_rows[128 x 576] . Q^T      (TMEM, fp32)
+//       A = gathered rows, K-major, 9 chunks of 64 dims (128-byte swizzle);
+//       B = the query's 64 heads, K-major; 36 tcgen05.mma kind::f16, K = 16.
+//   softmax (4 warps, one TMEM lane = one row per thread): per-head tile max
+//       by a transposing butterfly over the warp plus a 4-warp exchange;
+//       running max kept per head, raised only when a tile exceeds it by more
+//       than 2^8, in which case O is rescaled in TMEM; P = 2^(z - m) in bf16.
+//   PV  O^T[512 dv x 64 heads] += V^T[512 x 128 rows] . P^T[128 rows x 64]
 //       A = V^T (the first 512 dims of the same rows, MN-major), B = P^T
-//       (K-major, one 128-byte line per head); 4 blocks of 128 dv, hi and lo.
-// The rows of two tiles are resident at once (two buffers), and the MMA warp
-// issues QK of tile u before PV of tile u-1: the gathers of the next tile,
-// the tensor cores and the softmax of the current tile run at the same time.
+//       (MN-major, one 128-byte row per KV row); 4 blocks of 128 dv.
+// P is rounded to bf16 as hi + lo (two PV MMAs) and the softmax denominators
+// sum exactly the values the MMA multiplies, so the only rounding left in the
+// output is the final bf16 store.
 // The tiles of all queries are laid end to end and split evenly over one CTA
 // per SM.  A query whose tiles span several CTAs leaves one unnormalised
 // partial (O, m, l) per CTA in the workspace and a second small kernel merges
 // them:  M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
 //
 // Warp roles (320 threads):
-//   warps 0-3 softmax (warps 0-1 own the 64 heads; all four rescale O and
-//   read it out of TMEM, one TMEM lane quadrant each);
-//   warps 4-7 producer: a tile's 9 chunks of 64 rows by 16-byte cp.async
-//   into the swizzled layout, 8 consecutive threads per 128-byte row chunk
-//   (rows of 1152 bytes anywhere in the pool); each chunk's full barrier is
-//   armed by the copies themselves, so the producer never waits for its
-//   own loads, only for a slot to be released;
+//   warps 0-3 softmax, and at the end of each query segment O out of TMEM;
+//   warps 4-7 producer: the tile's 9 chunks of 128 rows by 16-byte cp.async
+//   into the 128-byte swizzled layout, 8 consecutive threads per 128-byte
+//   row chunk (rows of 1152 bytes anywhere in the pool); the tile stays
+//   resident from QK to PV, each chunk slot refilled for the next tile as
+//   soon as its last MMA is done (chunk 8 right after QK, chunks 0-7 after
+//   their PV block);
 //   warp 8 TMEM owner and MMA issuer; warp 9 streams Q's chunks from L2 by
-//   TMA through a six-slot ring.
+//   TMA through a three-slot ring.
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
@@ -53,42 +50,37 @@ namespace {
 using namespace sm100;
 
 constexpr int kHq = 64, kDqk = 576, kDv = 512;
-constexpr int kRows = 64;                    // selected rows per tile (MMA N of QK)
-constexpr int kChunks = kDqk / 64;           // 9 chunks of 64 dims; the first 8 are V
-constexpr int kChunkBytes = kRows * 128;     // 64 rows x 128 B
-constexpr int kQRing = 4;                    // Q chunks in flight
-constexpr int kQChunkBytes = kHq * 128;      // 8 KB (M rows 0-63 of the A operand)
-constexpr int kPBytes = kHq * 128;           // P^T: one 128-byte line (64 rows) per head
-constexpr int kThreads = 352;
-constexpr int kPrefetchAhead = 3;  // tiles the L2 prefetch runs ahead of the producer
+constexpr int kRows = 128;
+constexpr int kChunks = kDqk / 64;           // 9 K chunks of 64 dims; the first 8 are V
+constexpr int kChunkBytes = kRows * 128;     // 64 dims x 128 rows, bf16
+constexpr int kQRing = 5;                    // Q chunks in flight
+constexpr int kQChunkBytes = kHq * 128;      // 8 KB
+constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
+constexpr int kThreads = 320;                // 4 softmax + 4 producer + MMA + Q loader warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // two 64-column S buffers (lanes = heads)
-constexpr uint32_t kColO = 128;  // four 64-column O^T blocks (lanes = dv)
+constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
+constexpr uint32_t kColO = 128;  // four 64-column O^T blocks
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxCtas = 160;
-constexpr uint32_t kIdescQK = instr_desc(128, kRows, 1, 1, 0, 0);
-constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 0);
+constexpr uint32_t kIdescQK = instr_desc(128, kHq, 1, 1, 0, 0);
+constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
 // Chunk order within a tile: chunk 8 (needed by QK only) first, because its
-// slot is the first one a tile releases.
+// slot is the first one the previous tile releases.
 __device__ __forceinline__ int chunk_at(int i) { return i == 0 ? 8 : i - 1; }
 
 struct __align__(1024) Smem {
-  uint8_t kv[2][kChunks][kChunkBytes];  // two tile buffers
-  uint8_t q[kQRing][kQChunkBytes];      // Q chunks streamed from L2
-  uint8_t phi[2][kPBytes];              // P^T per tile parity: bf16 part (phi[0]
-  uint8_t plo[2][kPBytes];              // is also the M rows 64-127 of the last Q
-                                        // slot), bf16 remainder
-  uint64_t kfull[2][kChunks], kempty[2][kChunks], qfull[kQRing], qempty[kQRing];
-  uint64_t sfull[2], sempty[2], vfull[2], pfull[2], pempty[2], ofull, ofree, smsync, prsync,
-      done;
-  unsigned long long vmask[2];  // usable rows of the tiles in the two buffers
-  int rowtab[kRows];            // physical rows of the producer's current tile
+  uint8_t kv[kChunks][kChunkBytes];  // the tile's rows, resident from QK to PV
+  uint8_t q[kQRing][kQChunkBytes];   // Q chunks streamed from L2
+  uint8_t phi[kPBytes];              // P^T, bf16 part
+  uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi)
+  uint64_t kfull[kChunks], kempty[kChunks], qfull[kQRing], qempty[kQRing];
+  uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done;
+  int rowtab[kRows];  // physical rows of the producer's current tile
   uint32_t tmem_base;
   int abort;
-  int prod_tile;         // tile the producer is on (read by the prefetcher)
-  int resc_tile[2];      // last tile (per S buffer) whose softmax raised a max
-  float fscale[2][kHq];  // per S buffer: O rescale factor of each head
-  float l_inv[kHq];
+  int rescale[2];
+  float redm[4][kHq], reds[4][kHq];
+  float m_used[kHq], fscale[kHq], l_run[kHq], l_inv[kHq];
 };
 
 struct Geo {
@@ -199,6 +191,27 @@ __device__ __forceinline__ void fail(Smem& sm, int* status) {
   flag_status(status, DSA_STATUS_TIMEOUT);
 }
 
+// Transposing butterfly over a warp: on entry v[0..31] hold one value per
+// column for this lane's row; returns, in lane l, the reduction over the 32
+// lanes (rows) of column l.  31 shuffles for 32 columns.
+template <bool kMax>
+__device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int o = 16 >> st;
+    const int n = 32 >> st;  // live values
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
@@ -219,6 +232,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                "r"(src_bytes)
                : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // One arrival on `bar` once every cp.async this thread has issued so far has
 // landed; the thread does not wait (the arrival counts toward the barrier's
 // expected count).  The consumer makes the data visible to the tensor cores
@@ -251,32 +265,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
-    sm.prod_tile = 0;
-    sm.resc_tile[0] = sm.resc_tile[1] = -1;
-    for (int b = 0; b < 2; ++b)
-      for (int i = 0; i < kChunks; ++i) {
-        mbar_init(&sm.kfull[b][i], 128);  // one copy-tracking arrival per producer thread
-        mbar_init(&sm.kempty[b][i], 1);
-      }
+    sm.rescale[0] = sm.rescale[1] = 0;
+    for (int i = 0; i < kChunks; ++i) {
+      mbar_init(&sm.kfull[i], 128);
+      mbar_init(&sm.kempty[i], 1);
+    }
     for (int i = 0; i < kQRing; ++i) {
       mbar_init(&sm.qfull[i], 1);
       mbar_init(&sm.qempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.sfull[i], 1);
-      mbar_init(&sm.sempty[i], kHq);
-      mbar_init(&sm.vfull[i], 1);
+      mbar_init(&sm.sempty[i], 128);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.pfull[i], 128);
-      mbar_init(&sm.pempty[i], 1);
-    }
+    mbar_init(&sm.pfull, 128);
+    mbar_init(&sm.pempty, 1);
     mbar_init(&sm.ofull, 1);
     mbar_init(&sm.ofree, 128);
     mbar_init(&sm.smsync, 128);
     mbar_init(&sm.prsync, 128);
     mbar_init(&sm.done, 1);
     fence_mbar_init();
+  }
+  if (threadIdx.x < kHq) {
+    sm.m_used[threadIdx.x] = -INFINITY;
+    sm.l_run[threadIdx.x] = 0.0f;
+    sm.fscale[threadIdx.x] = 1.0f;
   }
   if (warp == 8) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -294,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each 128-byte row chunk is copied by 8 consecutive threads (16 B each),
     // so a warp instruction moves four whole rows; thread t copies granule
     // t % 8 of rows t / 8 + 16 i.  The tile's physical rows are looked up
-    // once (threads 0-63: one row each) into a shared table.
+    // once (thread t: row t) into a shared table.  A chunk's full barrier
+    // is armed by the copies themselves, so the producer never waits for
+    // its own loads: every slot is refilled as soon as it is released.
     const int pt = threadIdx.x - 128;
     const int gq = pt & 7, r0 = pt >> 3;
     const char* kv = reinterpret_cast<const char*>(a.kp);
@@ -303,49 +319,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walker w;
     w.init(a, g, r_first, r_last);
     int u = 0;
-    int p_cur = (w.ok && pt < kRows) ? sel_pos(a, w.s, (long long)w.t * kRows + pt) : -1;
+    int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + pt) : -1;
     while (w.ok && ok) {
-      const int bufi = u & 1;
-      const long long row_cur = pt < kRows ? pos_row(a, w.s, p_cur, false) : -1;
+      const long long row_cur = pos_row(a, w.s, p_cur, false);
       Walker nx = w;
       nx.next(a, g);
-      const int p_next =
-          (nx.ok && pt < kRows) ? sel_pos(a, nx.s, (long long)nx.t * kRows + pt) : -1;
+      const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + pt) : -1;
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
-      if (pt == 0) *(volatile int*)&sm.prod_tile = u;
-      if (pt < kRows) sm.rowtab[pt] = (int)row_cur;
+      sm.rowtab[pt] = (int)row_cur;
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
-      int rows[kRows / 16];
-#pragma unroll
-      for (int k = 0; k < kRows / 16; ++k) rows[k] = sm.rowtab[r0 + 16 * k];
-      // usable rows of this tile for the softmax (bit r: row r)
-      unsigned long long vmask = 0;
-      if (pt < 32) {
-        const unsigned lo = __ballot_sync(0xffffffffu, sm.rowtab[pt] >= 0);
-        const unsigned hi = __ballot_sync(0xffffffffu, sm.rowtab[pt + 32] >= 0);
-        vmask = ((unsigned long long)hi << 32) | lo;
-      }
       for (int i = 0; i < kChunks && ok; ++i) {
         const int c = chunk_at(i);
-        if (u >= 2 && !warp_wait(&sm.kempty[bufi][c], ((u >> 1) - 1) & 1, &sm.abort)) {
-          ok = false;
-          break;
-        }
-        if (i == 1 && pt == 0) {
-          // chunk 0's slot is released by the PV of this buffer's previous
-          // tile, after the softmax finished with its mask: the mask is free
-          sm.vmask[bufi] = vmask;
-          mbar_arrive(&sm.vfull[bufi]);
-        }
-        uint8_t* base = sm.kv[bufi][c];
+        if (u > 0 && !warp_wait(&sm.kempty[c], (u - 1) & 1, &sm.abort)) { ok = false; break; }
+        uint8_t* base = sm.kv[c];
 #pragma unroll
         for (int k = 0; k < kRows / 16; ++k) {
           const int r = r0 + 16 * k;
-          const int prow = rows[k];
+          const int prow = sm.rowtab[r];
           const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + c * 128 + gq * 16 : kv;
           cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
         }
-        cp_async_arrive(&sm.kfull[bufi][c]);
+        cp_async_arrive(&sm.kfull[c]);
       }
       p_cur = p_next;
       w = nx;
@@ -353,51 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait<0>();
     if (!ok) fail(sm, a.status);
-  } else if (warp == 10) {
-    // --------------------------------------------------------- L2 prefetch --
-    // The rows of the next tiles are pulled into L2 (one bulk prefetch per
-    // 1152-byte row) a few tiles ahead of the producer, so that its copies,
-    // which can only be in flight for one tile buffer, see L2 latency rather
-    // than HBM latency under load.  A hint only: on a stall it just stops.
-    const char* kv = reinterpret_cast<const char*>(a.kp);
-    // the Q rows of this CTA's queries first (contiguous, 64 x 1152 bytes
-    // each): every tile streams its query's Q chunks again
-    {
-      const char* qb = reinterpret_cast<const char*>(a.q);
-      const long long qbytes = (long long)kHq * kDqk * 2;
-      for (int r = r_first; r <= r_last; ++r)
-        for (long long o = (long long)lane * 4096; o < qbytes; o += 32 * 4096) {
-          const long long n = qbytes - o < 4096 ? qbytes - o : 4096;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qb + (size_t)r * qbytes + o),
-                       "r"((uint32_t)n)
-                       : "memory");
-        }
-    }
-    Walker w;
-    w.init(a, g, r_first, r_last);
-    int u = 0;
-    const uint64_t t0 = globaltimer_ns();
-    bool live = true;
-    while (w.ok && live) {
-      while (u > *(volatile int*)&sm.prod_tile + kPrefetchAhead) {
-        if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > 2000000000ull) {
-          live = false;
-          break;
-        }
-        __nanosleep(256);
-      }
-      if (!live) break;
-      for (int j = lane; j < kRows; j += 32) {
-        const long long row = pos_row(a, w.s, sel_pos(a, w.s, (long long)w.t * kRows + j), false);
-        if (row >= 0) {
-          const char* src = kv + (size_t)row * (kDqk * 2);
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(kDqk * 2)
-                       : "memory");
-        }
-      }
-      w.next(a, g);
-      ++u;
-    }
   } else if (warp == 9) {
     // ----------------------------------------------------------- Q loader --
     if (lane == 0) {
@@ -421,94 +370,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer --
-    // Two cursors, served as their inputs arrive: PV of the oldest tile whose
-    // P^T is ready (first: it releases a KV buffer), else the next chunk of
-    // QK (up to two tiles ahead).  QK of the next tile thus runs while the
-    // softmax of the current one does, and PV never waits for later loads.
     if (lane == 0) {
-      struct TileInfo { int seg; bool first, last; };
-      TileInfo info[4];
+      int u = 0, sa = 0, qs = 0, cur_r = -1;
+      bool ok = true;
       Walker w;
       w.init(a, g, r_first, r_last);
-      int u_qk = 0, i_qk = 0, qs = 0, cur_r = -1, sa = 0, u_pv = 0;
-      bool qk_all = !w.ok, ok = true;
-      uint64_t t_prog = globaltimer_ns();
-      uint32_t spins = 0;
-      while (ok && !(qk_all && u_pv == u_qk)) {
-        bool prog = false;
-        if (u_pv < u_qk) {
-          const TileInfo ti = info[u_pv & 3];
-          const int pb = u_pv & 1;
-          if (mbar_try_wait(&sm.pfull[pb], (u_pv >> 1) & 1) &&
-              (!ti.first || ti.seg == 0 || mbar_try_wait(&sm.ofree, (ti.seg - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t ph = smem_u32(sm.phi[pb]), pl = smem_u32(sm.plo[pb]);
-            for (int blk = 0; blk < kDv / 128; ++blk) {
-              const uint32_t v0 = smem_u32(sm.kv[pb][2 * blk]);  // chunks 2blk, 2blk+1: 8 KB apart
-              const uint32_t d = tbase + kColO + 64 * blk;
-#pragma unroll
-              for (int k = 0; k < kRows / 16; ++k) {
-                const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
-                mma_f16(d, va, smem_desc(ph + 32 * k, 16, 1024, kSwizzle128B), kIdescPV,
-                        (ti.first && k == 0) ? 0u : 1u);
-                mma_f16(d, va, smem_desc(pl + 32 * k, 16, 1024, kSwizzle128B), kIdescPV, 1u);
-              }
-              mma_commit(&sm.kempty[pb][2 * blk]);
-              mma_commit(&sm.kempty[pb][2 * blk + 1]);
-            }
-            mma_commit(&sm.pempty[pb]);
-            if (ti.last) mma_commit(&sm.ofull);
-            ++u_pv;
-            prog = true;
+      while (w.ok && ok) {
+        const bool first = (w.t == w.s.t0), last = (w.t == w.s.act_end - 1);
+        if (w.r != cur_r) {
+          cur_r = w.r;
+          ++sa;
+        }
+        if (!mbar_wait(&sm.sempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dS = tbase + kColS + 64 * (u & 1);
+        for (int i = 0; i < kChunks; ++i, ++qs) {
+          const int c = chunk_at(i), slot = qs % kQRing;
+          if (!mbar_wait(&sm.qfull[slot], (qs / kQRing) & 1, &sm.abort) ||
+              !mbar_wait(&sm.kfull[c], u & 1, &sm.abort)) {
+            ok = false;
+            break;
           }
-        }
-        if (!prog && !qk_all && u_qk < u_pv + 2) {
-          const int bufi = u_qk & 1;
-          const int c = chunk_at(i_qk), slot = qs % kQRing;
-          // S buffer free (the softmax of tile u_qk - 2 has read it), then
-          // this chunk's Q and rows
-          bool ready = i_qk > 0 || mbar_try_wait(&sm.sempty[bufi], ((u_qk >> 1) & 1) ^ 1);
-          ready = ready && mbar_try_wait(&sm.qfull[slot], (qs / kQRing) & 1) &&
-                  mbar_try_wait(&sm.kfull[bufi][c], (u_qk >> 1) & 1);
-          if (ready) {
-            if (i_qk == 0) {
-              if (w.r != cur_r) {
-                cur_r = w.r;
-                ++sa;
-              }
-              info[u_qk & 3] = TileInfo{sa - 1, w.t == w.s.t0, w.t == w.s.act_end - 1};
-            }
-            fence_proxy_async_smem();  // the copies' writes, seen by the tensor cores
-            tc_fence_after();
-            const uint32_t dS = tbase + kColS + 64 * bufi;
-            const uint32_t a0 = smem_u32(sm.q[slot]), b0 = smem_u32(sm.kv[bufi][c]);
+          fence_proxy_async_smem();  // the copies' writes, seen by the tensor cores
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sm.kv[c]), b0 = smem_u32(sm.q[slot]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16(dS, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B),
-                      smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B), kIdescQK,
-                      (i_qk + k) > 0 ? 1u : 0u);
-            mma_commit(&sm.qempty[slot]);
-            if (c == kChunks - 1) mma_commit(&sm.kempty[bufi][c]);  // QK only
-            ++qs;
-            if (++i_qk == kChunks) {
-              mma_commit(&sm.sfull[bufi]);
-              i_qk = 0;
-              ++u_qk;
-              w.next(a, g);
-              qk_all = !w.ok;
-            }
-            prog = true;
+          for (int k = 0; k < 4; ++k)
+            mma_f16(dS, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B),
+                    smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B), kIdescQK,
+                    (i + k) > 0 ? 1u : 0u);
+          mma_commit(&sm.qempty[slot]);
+          if (c == kChunks - 1) mma_commit(&sm.kempty[c]);  // QK only
+        }
+        if (!ok) break;
+        mma_commit(&sm.sfull[u & 1]);
+        // PV of this tile once the softmax has written P^T
+        if (!mbar_wait(&sm.pfull, u & 1, &sm.abort)) { ok = false; break; }
+        if (first && sa > 1 && !mbar_wait(&sm.ofree, (sa - 2) & 1, &sm.abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        for (int blk = 0; blk < kDv / 128; ++blk) {
+          const uint32_t v0 = smem_u32(sm.kv[2 * blk]);  // chunks 2blk, 2blk+1 are 16 KB apart
+          const uint32_t d = tbase + kColO + 64 * blk;
+#pragma unroll
+          for (int k = 0; k < kRows / 16; ++k) {
+            const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
+            mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+                    (first && k == 0) ? 0u : 1u);
+            mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
           }
+          mma_commit(&sm.kempty[2 * blk]);
+          mma_commit(&sm.kempty[2 * blk + 1]);
         }
-        if (prog) {
-          spins = 0;
-        } else if ((++spins & 255u) == 0) {
-          // bounded: give up after 2 s without progress, or when another
-          // role has
-          const uint64_t now = globaltimer_ns();
-          if (spins == 256) t_prog = now;
-          if (sm.abort || now - t_prog > 2000000000ull) ok = false;
-        }
+        mma_commit(&sm.pempty);
+        if (last) mma_commit(&sm.ofull);
+        ++u;
+        w.next(a, g);
       }
       if (!ok) fail(sm, a.status);
       mma_commit(&sm.done);
@@ -516,17 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax + finalize --
-    // Thread h < 64 (warps 0-1) owns head h: its S row is TMEM lane h.  All
-    // four warps take part in rescaling O^T and in reading it out (lane = dv
-    // within a 128-dv block).  Loops over 32-column groups stay rolled.
-    const int t = threadIdx.x;
-    const bool owner = t < kHq;
+    // Thread = TMEM lane = row of the tile (and dv lane of O at the end).
+    // The loops over 32-column groups stay rolled: this code runs once per
+    // tile, so it has to stay small enough to be fetched quickly.
+    const int row = threadIdx.x;
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float c = a.scale_log2;
     int u = 0, sa = 0;
     uint32_t sp = 0;
     bool ok = true;
-    float m = -INFINITY, l = 0.0f;  // running max (log2 units) and sum of head t
     for (int r = r_first; r <= r_last && ok; ++r) {
       const Seg s = make_seg(a, g, r);
       const int pslot = 2 * blockIdx.x + (((long long)r * g.Tq > g.lo) ? 1 : 0);
@@ -535,61 +450,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = a.out + (size_t)r * kHq * kDv;
       if (s.active() == 0) {
         if (s.complete) {
-          for (int i = t; i < kHq * kDv; i += 128) out[i] = __float2bfloat16(0.0f);
-          if (a.lse && owner) a.lse[(size_t)r * kHq + t] = -INFINITY;
-        } else if (owner) {
-          pml[2 * t] = -INFINITY;
-          pml[2 * t + 1] = 0.0f;
+          for (int i = row; i < kHq * kDv; i += 128) out[i] = __float2bfloat16(0.0f);
+          if (a.lse && row < kHq) a.lse[(size_t)r * kHq + row] = -INFINITY;
+        } else if (row < kHq) {
+          pml[2 * row] = -INFINITY;
+          pml[2 * row + 1] = 0.0f;
         }
         continue;
       }
-      for (int tt = s.t0; tt < s.act_end; ++tt) {
-        const int bufi = u & 1;
-        float f = 1.0f;
-        unsigned long long vm = 0;
-        const uint32_t ta = tbase + lanes + kColS + 64 * bufi;
-        if (owner) {
-          if (!warp_wait(&sm.sfull[bufi], (u >> 1) & 1, &sm.abort) ||
-              !warp_wait(&sm.vfull[bufi], (u >> 1) & 1, &sm.abort)) {
-            ok = false;
-          } else {
-            tc_fence_after();
-            vm = sm.vmask[bufi];
-            // pass 1: the tile's max for this head
-            float mt = -INFINITY;
+      // validity of this thread's row is looked up one tile ahead
+      bool valid_next = pos_row(a, s, sel_pos(a, s, (long long)s.t0 * kRows + row), true) >= 0;
+      bool pend_l = false;  // reds hold a tile's sums not yet added to l_run
+      for (int t = s.t0; t < s.act_end; ++t) {
+        const bool valid = valid_next;
+        if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ta = tbase + lanes + kColS + 64 * (u & 1);
+        // pass 1: per-head maximum of the tile
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint32_t raw[32];
-              tmem_ld_32cols(ta + 32 * half, raw);
-              tmem_wait_ld();
-              const unsigned vb = (unsigned)(vm >> (32 * half));
+        for (int half = 0; half < 2; ++half) {
+          uint32_t raw[32];
+          tmem_ld_32cols(ta + 32 * half, raw);
+          tmem_wait_ld();
+          float v[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                mt = fmaxf(mt, ((vb >> j) & 1u) ? __uint_as_float(raw[j]) * c : -INFINITY);
+          for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
+          sm.redm[warp][32 * half + lane] = butterfly32<true>(v, lane);
+        }
+        if (t + 1 < s.act_end)
+          valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
+        if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
+        if (row < kHq) {
+          // thread h owns head h: the previous tile's sums, then the new max
+          const int h = row;
+          if (pend_l)
+            sm.l_run[h] = sm.l_run[h] * sm.fscale[h] +
+                          ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
+          const float mt = fmaxf(fmaxf(sm.redm[0][h], sm.redm[1][h]),
+                                 fmaxf(sm.redm[2][h], sm.redm[3][h]));
+          const float mo = sm.m_used[h];
+          float mn = mo, f = 1.0f;
+          if (mt > mo + kRescaleLog2 || (mo == -INFINITY && mt > -INFINITY)) {
+            mn = mt;
+            if (mo > -INFINITY) {
+              f = exp2f(mo - mn);
+              sm.rescale[u & 1] = 1;
             }
-            if (mt > m + kRescaleLog2 || (m == -INFINITY && mt > -INFINITY)) {
-              if (m > -INFINITY) {
-                f = exp2f(m - mt);
-                sm.resc_tile[bufi] = u;
-              }
-              m = mt;
-            }
-            sm.fscale[bufi][t] = f;
           }
+          sm.m_used[h] = mn;
+          sm.fscale[h] = f;
         }
-        if (!group_sync(&sm.smsync, sp, &sm.abort) || !ok) { ok = false; break; }
-        // fscale and the flag are per S buffer: the next writer of this
-        // buffer's entries (tile u + 2) starts only after every thread has
-        // passed tile u + 1's barrier
-        const bool resc = sm.resc_tile[bufi] == u;
-        // O changes only after PV of the previous tile is done (u > 0 here:
-        // a segment's first tile never rescales)
-        if (resc && !warp_wait(&sm.pempty[bufi ^ 1], ((u - 1) >> 1) & 1, &sm.abort)) {
-          ok = false;
-          break;
-        }
-        // this P^T buffer is free once PV of tile u - 2 is done
-        if (!warp_wait(&sm.pempty[bufi], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
+        const bool resc = sm.rescale[u & 1] != 0;
+        if (row == 0) sm.rescale[(u + 1) & 1] = 0;
+        // the previous PV must be done before P^T (and, if needed, O) change
+        if (!warp_wait(&sm.pempty, (u & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         if (resc) {
 #pragma unroll 1
@@ -600,63 +515,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              raw[i] = __float_as_uint(__uint_as_float(raw[i]) * sm.fscale[bufi][32 * (q & 1) + i]);
+              raw[i] = __float_as_uint(__uint_as_float(raw[i]) * sm.fscale[32 * (q & 1) + i]);
             tmem_st_32cols(to, raw);
           }
           tmem_wait_st();
         }
-        if (owner) {
-          // pass 2: P = 2^(z - m) as bf16 hi + lo, one 128-byte line of P^T
-          // per head; l sums exactly what the MMAs multiply.  S is read a
-          // second time (it stays in TMEM until sempty).
-          float lt = 0.0f;
-          uint8_t* rh = sm.phi[bufi] + t * 128;
-          uint8_t* rl = sm.plo[bufi] + t * 128;
+        // pass 2: P = 2^(z - m) as bf16 hi + lo into this row of P^T; the
+        // per-head sums add exactly the values the two PV MMAs multiply
+        uint8_t* rh = sm.phi + row * 128;
+        uint8_t* rl = sm.plo + row * 128;
 #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t raw[32];
-            tmem_ld_32cols(ta + 32 * half, raw);
-            tmem_wait_ld();
-            const unsigned vb = (unsigned)(vm >> (32 * half));
-            uint32_t hw[16], lw[16];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t raw[32];
+          tmem_ld_32cols(ta + 32 * half, raw);
+          tmem_wait_ld();
+          float v[32];
+          uint32_t hw[16], lw[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              // branch-free: an unusable row gives 2^-inf = 0 (a usable row
-              // makes the running max finite)
-              const float p0 =
-                  ex2_approx(((vb >> j) & 1u) ? __uint_as_float(raw[j]) * c - m : -INFINITY);
-              const float p1 = ex2_approx(
-                  ((vb >> (j + 1)) & 1u) ? __uint_as_float(raw[j + 1]) * c - m : -INFINITY);
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-              const float2 hf = __bfloat1622float2(hi);
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-              const float2 lf = __bfloat1622float2(lo);
-              lt += (hf.x + lf.x) + (hf.y + lf.y);
-              hw[j / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-              lw[j / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int off = ((4 * half + k) ^ (t & 7)) << 4;
-              *reinterpret_cast<uint4*>(rh + off) =
-                  make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-              *reinterpret_cast<uint4*>(rl + off) =
-                  make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
-            }
+          for (int i = 0; i < 32; i += 2) {
+            // branch-free: an unusable row gives 2^-inf = 0 (a usable row makes
+            // every head's running max finite)
+            const float m0 = sm.m_used[32 * half + i], m1 = sm.m_used[32 * half + i + 1];
+            const float p0 = ex2_approx(valid ? __uint_as_float(raw[i]) * c - m0 : -INFINITY);
+            const float p1 = ex2_approx(valid ? __uint_as_float(raw[i + 1]) * c - m1 : -INFINITY);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+            const float2 lf = __bfloat1622float2(lo);
+            v[i] = hf.x + lf.x;
+            v[i + 1] = hf.y + lf.y;
+            hw[i / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+            lw[i / 2] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          l = l * f + lt;
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(&sm.sempty[bufi]);  // S buffer read for the last time
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int off = ((4 * half + k) ^ (row & 7)) << 4;
+            *reinterpret_cast<uint4*>(rh + off) =
+                make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+            *reinterpret_cast<uint4*>(rl + off) =
+                make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          }
+          sm.reds[warp][32 * half + lane] = butterfly32<false>(v, lane);
         }
+        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.pfull[bufi]);  // all four warps: P^T written and O rescaled
+        mbar_arrive(&sm.sempty[u & 1]);
+        mbar_arrive(&sm.pfull);
+        pend_l = true;
         ++u;
       }
       if (!ok) break;
       // ---- finalize the query segment: O out of TMEM ----
-      if (owner) sm.l_inv[t] = l > 0.0f ? 1.0f / l : 0.0f;
-      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // last tile's sums
+      if (row < kHq) {
+        const int h = row;
+        const float l = sm.l_run[h] * sm.fscale[h] +
+                        ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
+        sm.l_run[h] = l;
+        sm.l_inv[h] = l > 0.0f ? 1.0f / l : 0.0f;
+      }
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // l_run final
       if (!warp_wait(&sm.ofull, sa & 1, &sm.abort)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -665,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t raw[32];
         tmem_ld_32cols(tbase + lanes + kColO + 64 * blk + 32 * half, raw);
         tmem_wait_ld();
-        const int dv = blk * 128 + t;
+        const int dv = blk * 128 + row;
         if (s.complete) {
           __nv_bfloat16* o = out + (size_t)(32 * half) * kDv + dv;
 #pragma unroll
@@ -677,20 +595,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[(size_t)i * kDv] = __uint_as_float(raw[i]);
         }
       }
-      if (owner) {
+      if (row < kHq) {
+        const float m = sm.m_used[row], l = sm.l_run[row];
         if (s.complete) {
           if (a.lse)
-            a.lse[(size_t)r * kHq + t] = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            a.lse[(size_t)r * kHq + row] =
+                l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
         } else {
-          pml[2 * t] = m;
-          pml[2 * t + 1] = l;
+          pml[2 * row] = m;
+          pml[2 * row + 1] = l;
         }
-        m = -INFINITY;
-        l = 0.0f;
       }
       tc_fence_before();
       mbar_arrive(&sm.ofree);
-      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // l_inv reusable
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // stats read
+      if (row < kHq) {
+        sm.m_used[row] = -INFINITY;
+        sm.l_run[row] = 0.0f;
+        sm.fscale[row] = 1.0f;
+      }
       ++sa;
       ok = ok && !sm.abort;
     }
