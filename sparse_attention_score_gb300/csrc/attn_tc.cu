@@ -232,7 +232,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // One arrival on `bar` once every cp.async this thread has issued so far has
 // landed; the thread does not wait (the arrival counts toward the barrier's
 // expected count).  The consumer makes the data visible to the tensor cores
@@ -645,6 +644,7 @@ __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, cons
   const int h0 = blockIdx.x * 8;
   __shared__ float wgt[8][kMaxCtas + 1], lpart[8][kMaxCtas + 1];
   __shared__ float lsum[8], mmax[8];
+  __shared__ int pslot[kMaxCtas + 1];
   const int ns = c1 - c0 + 1;
   // (m, l) of every slot and head of this group, loaded all at once
   for (int i = threadIdx.x; i < ns * 8; i += blockDim.x) {
@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, cons
         __ldcg(reinterpret_cast<const float2*>(part_ml + ((size_t)ps * kHq + h0 + hh) * 2));
     wgt[hh][i / 8] = ml.y > 0.0f ? ml.x : -INFINITY;
     lpart[hh][i / 8] = ml.y;
+    if (hh == 0) pslot[i / 8] = ps;
   }
   __syncthreads();
   {
@@ -677,20 +678,36 @@ __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, cons
   }
   __syncthreads();
   // thread t owns outputs t + 256 k (k < 16): head k/2, dv t + 256 (k & 1);
-  // every slot's 16 loads are independent, so they overlap
+  // slots are taken two at a time, so 32 independent loads are in flight
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-  for (int cc = c0; cc <= c1; ++cc) {
-    const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-    const float* src = part_o + ((size_t)ps * kHq + h0) * kDv + threadIdx.x;
-    float val[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) val[k] = __ldcg(src + (size_t)(k >> 1) * kDv + 256 * (k & 1));
+  int j = 0;
+  for (; j + 1 < ns; j += 2) {
+    const float* s0 = part_o + ((size_t)pslot[j] * kHq + h0) * kDv + threadIdx.x;
+    const float* s1 = part_o + ((size_t)pslot[j + 1] * kHq + h0) * kDv + threadIdx.x;
+    float v0[16], v1[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const float w = wgt[k >> 1][cc - c0];
-      acc[k] = w > 0.0f ? fmaf(w, val[k], acc[k]) : acc[k];
+      v0[k] = __ldcg(s0 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
+      v1[k] = __ldcg(s1 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float w0 = wgt[k >> 1][j], w1 = wgt[k >> 1][j + 1];
+      acc[k] = w0 > 0.0f ? fmaf(w0, v0[k], acc[k]) : acc[k];
+      acc[k] = w1 > 0.0f ? fmaf(w1, v1[k], acc[k]) : acc[k];
+    }
+  }
+  if (j < ns) {
+    const float* s0 = part_o + ((size_t)pslot[j] * kHq + h0) * kDv + threadIdx.x;
+    float v0[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v0[k] = __ldcg(s0 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float w0 = wgt[k >> 1][j];
+      acc[k] = w0 > 0.0f ? fmaf(w0, v0[k], acc[k]) : acc[k];
     }
   }
 #pragma unroll
