@@ -173,18 +173,46 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && lo < hi) {
-      Cursor c;
-      c.seek(s, nq, lo);
+      // The block-table entries of tile i + 1 are loaded while tile i waits
+      // for its stage, so their latency is off the issue path.
+      struct TileLoad {
+        int r, pages;
+        long long p0;
+        int page[2];
+      };
+      Cursor ca;
+      ca.seek(s, nq, lo);
+      int acur = -1;
+      Query aq{};
+      auto look = [&](int item) {
+        TileLoad t;
+        ca.advance(s, item);
+        if (ca.r != acur) {
+          acur = ca.r;
+          aq = query_info(a, acur);
+        }
+        t.r = acur;
+        t.p0 = (long long)(item - s.prefix[acur]) * kTileRows;
+        const long long rows = min((long long)kTileRows, aq.n - t.p0);
+        t.pages = (int)((rows + 63) / 64);
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          int page = 0;
+          if (pg < t.pages) page = __ldg(&a.lay.bt[(long long)aq.b * a.lay.maxb + t.p0 / 64 + pg]);
+          t.page[pg] = page;
+        }
+        return t;
+      };
+      TileLoad nxt = look(lo);
       int cur = -1, nb = 0, stage = 0;
       uint32_t phase = 0;
-      Query q{};
       uint32_t issued_parity[kStages];
       int issued = 0;
       for (int item = lo; item < hi; ++item) {
-        c.advance(s, item);
-        if (c.r != cur) {
-          cur = c.r;
-          q = query_info(a, cur);
+        const TileLoad t = nxt;
+        if (item + 1 < hi) nxt = look(item + 1);
+        if (t.r != cur) {
+          cur = t.r;
           const int slot = nb & 1;
           if (nb >= 2 && !mbar_wait(&s.bempty[slot], ((nb >> 1) - 1) & 1, &s.abort)) {
             fail(s, a.status);
@@ -194,17 +222,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           tma_load_2d(s.b[slot], &map_q, &s.bfull[slot], 0, cur * kHeads);
           ++nb;
         }
-        const long long p0 = (long long)(item - s.prefix[cur]) * kTileRows;
-        const long long rows = min((long long)kTileRows, q.n - p0);
-        const int pages = (int)((rows + 63) / 64);
         if (!mbar_wait(&s.empty[stage], phase ^ 1, &s.abort)) {
           fail(s, a.status);
           break;
         }
-        mbar_arrive_expect_tx(&s.full[stage], pages * kPageBytes);
-        for (int pg = 0; pg < pages; ++pg) {
-          const long long slot = p0 / 64 + pg;
-          int page = __ldg(&a.lay.bt[(long long)q.b * a.lay.maxb + slot]);
+        mbar_arrive_expect_tx(&s.full[stage], t.pages * kPageBytes);
+        for (int pg = 0; pg < t.pages; ++pg) {
+          int page = t.page[pg];
           if (page < 0 || page >= a.lay.nb) page = 0;  // epilogue flags and masks it
           tma_load_2d(s.a[stage] + pg * kPageBytes, &map_k, &s.full[stage], 0, page * 64);
         }
