@@ -320,6 +320,7 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
         torch.cuda.synchronize()
         stage[:, k] = [a_.elapsed_time(b_) for a_, b_ in sev]
     status = pipe.status()
+    cache_write = measure_cache_write(dsa, case, d, layout, dev, flush, steps)
 
     e2e = None
     if do_e2e:
@@ -332,7 +333,51 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
         torch.distributed.barrier()
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
                 launches=int(launches), launches_per=launches_per, clocks=clocks, status=status,
-                e2e=e2e, graph=graphs["step"])
+                e2e=e2e, graph=graphs["step"], cache_write=cache_write)
+
+
+def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
+    """The cache write that feeds the step, timed on its own: decode appends
+    each sequence's newest row, prefill stores the whole prompt.  The rows
+    written are the rows already cached there (read back through the block
+    table), so the cache the step reads is unchanged.  Algorithmic bytes: each
+    K/V row and indexer-key row read once and written once."""
+    import torch
+    if case.kind == "decode":
+        seq = torch.arange(case.B, dtype=torch.int32, device=dev)
+        pos = (d.seq_lens - 1).to(torch.int32)
+    else:
+        seq = torch.zeros(case.Nq, dtype=torch.int32, device=dev)
+        pos = d.q_pos.clone()
+    pl, sl = pos.long(), seq.long()
+    phys = d.block_table.long()[sl, pl // case.bs] * case.bs + pl % case.bs
+    kv_rows = d.k_pool.view(-1, d.k_pool.shape[-1])[phys].contiguous()
+    ki_rows = d.kidx_pool.view(-1, d.kidx_pool.shape[-1])[phys].contiguous()
+    ws = dsa.workspace(dsa.cache_write_workspace_size(), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        dsa.cache_write(layout, seq, pos, ws, kv_new=kv_rows, kv_pool=d.k_pool, kidx_new=ki_rows,
+                        kidx_pool=d.kidx_pool)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev])) * 1e3
+    n = int(seq.shape[0])
+    row_bytes = kv_rows.shape[1] * kv_rows.element_size() + ki_rows.shape[1] * ki_rows.element_size()
+    nbytes = 2 * n * row_bytes
+    return {"rows": n, "bytes_per_row": int(row_bytes), "us": round(us, 2),
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "status": dsa.get_status(ws)}
 
 
 def run_e2e(case, d, pipe, graph, steps, dev, flush):
@@ -547,6 +592,7 @@ def main():
         "gpu_launches": res["launches"],
         "gpu_launches_per_step": res["launches_per"],
         "device_status": res["status"],
+        "cache_write": res["cache_write"],
     }
     if case.kind == "decode":
         frac = step_work / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
@@ -565,7 +611,8 @@ def main():
                "unit": unit_of(c2), "ms_per_step": r2["total_ms"] / st2, "steps": st2,
                "config": config_of(c2, world), "roofline": roof2,
                "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
-               "gpu_launches": r2["launches"], "clocks": r2["clocks"]}
+               "gpu_launches": r2["launches"], "clocks": r2["clocks"],
+               "cache_write": r2["cache_write"]}
         if c2.kind == "prefill":
             ideal_s = (algorithmic(c2)["index_flops"] / (peaks["bf16_tflops"] * 2e12) +
                        algorithmic(c2)["attn_flops"] / (peaks["bf16_tflops"] * 1e12))

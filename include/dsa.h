@@ -239,6 +239,38 @@ int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const
                             dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Cache write: store new rows into the paged caches -- a whole prompt after
+ * prefill, the appended token at each decode step.  Source: "Day-0
+ * Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
+ * Accelerators", section 4: the KV cache is written in the block layout, and
+ * the layout written during prefill must match exactly the gather addresses
+ * read during decode.  Row i goes to position pos[i] of sequence seq[i], i.e.
+ * physical row block_table[seq][pos / block_size] * block_size
+ * + pos % block_size -- the same mapping every gather above uses.
+ *
+ *  layout      paged layout (seq_lens is not read: the caller owns lengths)
+ *  seq, pos    [N] int32 sequence and position of each new row
+ *  kv_new      [N][row_elems] bf16 rows (K, or the latent K/V row), or NULL
+ *  row_elems   bf16 elements per row, a multiple of 8
+ *  kv_pool     physical rows of row_elems bf16, kv_row_stride elements apart
+ *              (a multiple of 8, >= row_elems)
+ *  kidx_new    [N][D_i] indexer-key rows of kidx_dtype, or NULL
+ *  kidx_pool   [num_blocks][block_size][D_i] of kidx_dtype
+ *  ws          workspace of dsa_cache_write_workspace_size() bytes
+ * Pointers 16-byte aligned.  Rows of the same physical row written twice in
+ * one call: one of them wins (unspecified which).
+ * Errors: DSA_ERR_INVALID for null pointers, N < 0, bad sizes, strides or
+ * alignment.  Device: a sequence outside [0, batch), a position outside the
+ * block table or a block id outside [0, num_blocks) skips that row and sets
+ * DSA_STATUS_BAD_BLOCK.
+ */
+size_t dsa_cache_write_workspace_size(void);
+int dsa_cache_write(const dsa_paged_layout* layout, const int32_t* seq, const int32_t* pos, int N,
+                    const void* kv_new, int row_elems, void* kv_pool, int64_t kv_row_stride,
+                    const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, void* ws,
+                    size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Utilities (no counterpart on the pages).
  * dsa_get_status: copy the status word of a workspace to *status (host), after
  *   the work queued on `stream` so far has finished (this call synchronises the

@@ -21,6 +21,10 @@ cites the passage it follows:
   third page, section 4: exact softmax attention over the gathered rows only.
 * the paged layout -- first page, section 3 (2): pages contiguous inside, an
   index table jumping between pages.
+* ``cache_write`` -- "Day-0 Adaptation of Ultra-Large-Scale MoE Models on
+  Heterogeneous AI Accelerators", section 4: new rows are written into the
+  KV cache in the block layout, at the rows the decode gather reads (plain
+  numpy, one row at a time).
 
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/`` against
 closed forms, invariants, library special cases and brute force; none of the
@@ -178,3 +182,35 @@ def sparse_attn(block_table, seq_lens, bs, num_blocks, q_seq, q, k_pool, v_pool,
     if rc != 0:
         raise OracleError(f"oracle_sparse_attn returned {rc}")
     return out, lse
+
+
+def cache_write(block_table, bs, num_blocks, seq, pos, new_rows, pool):
+    """(pool', bad): pool [NB, bs, W] with row i of new_rows [N, w <= W] stored
+    at position pos[i] of sequence seq[i]; bad is True when some row had no
+    valid destination (sequence outside the table, position past its row of
+    the table, or a page id outside [0, NB)) and was skipped.
+
+    "Day-0 Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
+    Accelerators", section 4 (KV cache write in the block layout; the layout
+    written must match the gather of decode), with the mapping of "Day-0
+    Adaptation of Trillion-Parameter MoE Models on Domestic GPUs", section 3
+    (2): position p lives in page block_table[b][p // bs], row p % bs.  Rows
+    are written in order, so of two rows with one destination the later wins.
+    """
+    bt = np.asarray(block_table)
+    out = np.array(pool, copy=True)
+    assert out.shape[0] == num_blocks and out.shape[1] == bs
+    new_rows = np.asarray(new_rows)
+    w = new_rows.shape[1]
+    bad = False
+    for i in range(len(seq)):
+        b, p = int(seq[i]), int(pos[i])
+        if b < 0 or b >= bt.shape[0] or p < 0 or p // bs >= bt.shape[1]:
+            bad = True
+            continue
+        page = int(bt[b, p // bs])
+        if page < 0 or page >= num_blocks:
+            bad = True
+            continue
+        out[page, p % bs, :w] = new_rows[i]
+    return out, bad

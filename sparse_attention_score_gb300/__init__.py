@@ -85,6 +85,8 @@ _sig("dsa_index_score_prefill", _i, [_LP, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _i
 _sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
 _sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_topk_noalloc", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp])
+_sig("dsa_cache_write_workspace_size", _sz, [])
+_sig("dsa_cache_write", _i, [_LP, _vp, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
 _sig("dsa_sparse_attn_decode", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i, _vp, _i, _f, _vp,
                                     _vp, _vp, _sz, _vp])
@@ -97,7 +99,8 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_index_score_prefill_workspace_size", "dsa_index_score_prefill",
            "dsa_topk_workspace_size",
            "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
-           "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill")
+           "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill",
+           "dsa_cache_write_workspace_size", "dsa_cache_write")
 
 
 def lib() -> ctypes.CDLL:
@@ -245,6 +248,29 @@ def sparse_attn_prefill(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, o
                                       _ptr(q_pos), Nq, _ptr(idx), idx.shape[1], float(sm_scale),
                                       _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "dsa_sparse_attn_prefill")
+
+
+def cache_write_workspace_size() -> int:
+    return int(_lib.dsa_cache_write_workspace_size())
+
+
+def cache_write(layout: PagedLayout, seq, pos, ws, kv_new=None, kv_pool=None, kidx_new=None,
+                kidx_pool=None, stream=None):
+    """Store row i of kv_new / kidx_new at position pos[i] of sequence seq[i] of
+    kv_pool / kidx_pool, through the block table (include/dsa.h, dsa_cache_write).
+
+    kv_new [N, row_elems] bf16 into kv_pool [NB, bs, stride >= row_elems];
+    kidx_new [N, D_i] into kidx_pool [NB, bs, D_i] (bf16 or FP8 E4M3).
+    """
+    N = int(seq.shape[0])
+    row_elems = int(kv_new.shape[-1]) if kv_new is not None else 0
+    stride = int(kv_pool.shape[-1]) if kv_pool is not None else 0
+    D_i = int(kidx_new.shape[-1]) if kidx_new is not None else 0
+    kdt = _elt_dtype(kidx_new) if kidx_new is not None else DSA_BF16
+    rc = _lib.dsa_cache_write(layout.c(), _ptr(seq), _ptr(pos), N, _ptr(kv_new), row_elems,
+                              _ptr(kv_pool), stride, _ptr(kidx_new), D_i, kdt, _ptr(kidx_pool),
+                              _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "dsa_cache_write")
 
 
 def get_status(ws, clear: bool = True, stream=None) -> int:

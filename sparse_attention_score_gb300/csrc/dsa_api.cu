@@ -170,6 +170,22 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
   return launch_topk(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t dsa_cache_write_workspace_size(void) { return kWsHeader; }
+
+int dsa_cache_write(const dsa_paged_layout* layout, const int32_t* seq, const int32_t* pos, int N,
+                    const void* kv_new, int row_elems, void* kv_pool, int64_t kv_row_stride,
+                    const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, void* ws,
+                    size_t ws_bytes, dsa_stream_t stream) {
+  LayoutDev lay;
+  int rc = check_layout(layout, &lay);
+  if (rc) return rc;
+  rc = check_ws(ws, ws_bytes, kWsHeader);
+  if (rc) return rc;
+  return cache_write(lay, seq, pos, N, kv_new, row_elems, kv_pool, (long long)kv_row_stride,
+                     kidx_new, D_i, kidx_dtype, kidx_pool, reinterpret_cast<int*>(ws),
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
 static int attn_common(const dsa_paged_layout* layout, const void* q, const void* k_pool,
                        int64_t k_row_stride, const void* v_pool, int64_t v_row_stride, int Hq,
                        int Dqk, int Dv, const int32_t* q_seq, const int32_t* q_pos, int Nq,

@@ -89,6 +89,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// cache_write.cu
+int cache_write(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, int N,
+                const void* kv_new, int row_elems, void* kv_pool, long long kv_row_stride,
+                const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, int* status,
+                cudaStream_t s);
+
 // host-side bookkeeping (dsa_api.cu)
 void count_launch(int n = 1);
 int set_error(int code, const std::string& msg);

@@ -416,3 +416,87 @@ def test_oracle_reports_bad_block_table():
     bt[0, 1] = c.num_blocks + 5
     with pytest.raises(oracle.OracleError):
         scores_of(c, block_table=bt)
+
+
+# ------------------------------------------------------------- cache write --
+def _logical_write_all(c, pool_src, bt, num_blocks, fill):
+    """Write every cached position of every sequence of c (rows read from
+    pool_src through c's own table) into a pool of `fill` laid out by bt."""
+    seq = np.concatenate([np.full(int(L), b, np.int32) for b, L in enumerate(c.seq_lens)])
+    pos = np.concatenate([np.arange(int(L), dtype=np.int32) for L in c.seq_lens])
+    rows = np.concatenate([logical_rows(c, pool_src, b) for b in range(c.B)])
+    dst = np.full((num_blocks, c.bs, pool_src.shape[-1]), fill, pool_src.dtype)
+    return seq, pos, rows, dst
+
+
+def test_cache_write_round_trip_through_the_page_view():
+    """Rows written one by one land where the page view (pages of the table,
+    reshaped to rows) reads them back; nothing else changes."""
+    c = _small_case("bf16")
+    seq, pos, rows, dst = _logical_write_all(c, c.k_pool, c.block_table, c.num_blocks, 0x7FC1)
+    out, bad = oracle.cache_write(c.block_table, c.bs, c.num_blocks, seq, pos, rows, dst)
+    assert not bad
+    for b in range(c.B):
+        np.testing.assert_array_equal(logical_rows(c, out, b), logical_rows(c, c.k_pool, b))
+    untouched = np.all(out.reshape(-1, out.shape[-1]) == 0x7FC1, axis=1).sum()
+    assert untouched == c.num_blocks * c.bs - int(c.seq_lens.sum())
+
+
+def test_cache_write_order_of_distinct_rows_is_irrelevant_and_last_duplicate_wins():
+    c = _small_case("fp8")
+    seq, pos, rows, dst = _logical_write_all(c, c.kidx_pool, c.block_table, c.num_blocks, 0)
+    a, _ = oracle.cache_write(c.block_table, c.bs, c.num_blocks, seq, pos, rows, dst)
+    perm = np.random.default_rng(5).permutation(seq.shape[0])
+    b, _ = oracle.cache_write(c.block_table, c.bs, c.num_blocks, seq[perm], pos[perm], rows[perm],
+                              dst)
+    np.testing.assert_array_equal(a, b)
+    two = np.stack([np.full(c.D_i, 3, np.uint8), np.full(c.D_i, 9, np.uint8)])
+    d2, _ = oracle.cache_write(c.block_table, c.bs, c.num_blocks, [1, 1], [5, 5], two, dst)
+    page = c.block_table[1, 0]
+    np.testing.assert_array_equal(d2[page, 5], two[1])
+
+
+def test_cache_write_skips_rows_without_a_destination_and_keeps_wide_rows_tails():
+    c = _small_case("bf16")
+    dst = np.full((c.num_blocks, c.bs, c.Dkv), 0x1234, np.uint16)
+    rows = np.arange(6 * 5, dtype=np.uint16).reshape(6, 5)       # 5 of Dkv columns
+    past = c.block_table.shape[1] * c.bs
+    unused = int(np.argmax(c.block_table[1] < 0)) * c.bs           # first page slot set to -1
+    assert c.block_table[1, unused // c.bs] < 0
+    seq = [-1, c.B, 0, 0, 1, 2]
+    pos = [0, 0, -1, past, unused, 3]
+    out, bad = oracle.cache_write(c.block_table, c.bs, c.num_blocks, seq, pos, rows, dst)
+    assert bad
+    page = c.block_table[2, 0]
+    np.testing.assert_array_equal(out[page, 3, :5], rows[5])
+    assert np.all(out[page, 3, 5:] == 0x1234)
+    changed = np.argwhere(np.any(out != dst, axis=-1))
+    assert changed.tolist() == [[page, 3]]
+
+
+def test_cache_written_at_prefill_serves_the_decode_gather():
+    """Prefill writes a prompt into pages of a fresh table; every stage read
+    through that table gives what it gives on the original cache (the block
+    layout written must match the gather that decode reads)."""
+    c = W.make_case(seed=13, seq_lens=(150, 77), bs=16, Hq=2, Dqk=24, Dv=16, latent=True,
+                    H_i=3, D_i=16, idx_dtype="fp8", K=40)
+    nb2 = c.num_blocks + 4
+    perm = np.random.default_rng(8).permutation(nb2).astype(np.int32)
+    bt2 = np.full_like(c.block_table, -1)
+    used = c.block_table >= 0
+    bt2[used] = perm[:int(used.sum())]
+    seq, pos, rows_k, dst_k = _logical_write_all(c, c.k_pool, bt2, nb2, 0)
+    _, _, rows_i, dst_i = _logical_write_all(c, c.kidx_pool, bt2, nb2, 0)
+    kp, bad_k = oracle.cache_write(bt2, c.bs, nb2, seq, pos, rows_k, dst_k)
+    ip, bad_i = oracle.cache_write(bt2, c.bs, nb2, seq, pos, rows_i, dst_i)
+    assert not bad_k and not bad_i
+    s1 = scores_of(c)
+    s2 = oracle.index_score(bt2, c.seq_lens, c.bs, nb2, c.q_seq, c.q_pos, c.q_idx, c.w, ip,
+                            code(c), c.max_len)
+    np.testing.assert_array_equal(s1, s2)
+    idx = oracle.topk(s1, c.n_elig, c.K)
+    o1, l1 = _attn(c, idx)
+    o2, l2 = oracle.sparse_attn(bt2, c.seq_lens, c.bs, nb2, c.q_seq, c.q, kp, kp, idx, c.sm_scale,
+                                Dv=c.Dv)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
