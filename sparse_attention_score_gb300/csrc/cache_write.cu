@@ -45,7 +45,7 @@ constexpr int kHeld = 4;
 // Every load of a row is issued before its destination is known: the source
 // granules depend only on the row number, so they travel while the
 // sequence / position / block-table chain resolves.
-__global__ void __launch_bounds__(kWarps * 32) k_cache_write(CacheWriteParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 5) k_cache_write(CacheWriteParams p) {
   grid_dependency_wait();
   launch_dependents();
   const int lane = threadIdx.x & 31;

@@ -54,10 +54,13 @@ class GpuRun:
         kind = "decode" if case.kind == "decode" else "prefill"
         self.pipe = self.dsa.Pipeline(self.layout, kind=kind, Nq=case.Nq, Hq=case.Hq, Dqk=case.Dqk,
                                       Dv=case.Dv, H_i=case.H_i, D_i=case.D_i, K=case.K, ld=ld,
-                                      device=device)
+                                      device=device,
+                                      prefill_seq=None if case.kind == "mixed" else 0)
 
     def scores(self):
         d, p = self.d, self.pipe
+        if self.case.kind == "mixed":
+            return self.scores_general()
         if self.case.kind == "decode":
             self.dsa.index_score(self.layout, d.q_idx, d.w, d.kidx_pool, p.scores, p.ws_index)
         else:

@@ -311,3 +311,74 @@ def test_prefill_indexer_query_subset_ragged_block():
     idx = g.topk().cpu().numpy()
     np.testing.assert_array_equal(idx, oracle.topk(s_ref, c.n_elig, c.K))
     assert g.status() == 0
+
+
+# ------------------------------------------------ mixed prefill/decode batch --
+def _mixed(seed, lens, nq, K):
+    return W.make_case("mixed", seed=seed, kind="mixed", seq_lens=lens, q_per_seq=nq, K=K,
+                       **LAT_SHAPES)
+
+
+def test_mixed_prefill_decode_batch_one_launch_per_stage():
+    """One batch holding a prefill chunk over an existing prefix, two decode
+    steps, a whole short prompt and a one-page prompt: each stage is one call
+    of the general entry points (explicit q_seq / q_pos)."""
+    need_gpu()
+    c = _mixed(600, (3000, 700, 5000, 129, 64), (100, 1, 1, 129, 64), 128)
+    g = GpuRun(c)
+    dsa = g.dsa
+    n0 = dsa.launch_count()
+    d = g.d
+    g.pipe.run(d.q, d.q_idx, d.w, d.kidx_pool, d.k_pool, d.v_pool, c.sm_scale,
+               n_eligible=d.n_elig, q_seq=d.q_seq, q_pos=d.q_pos)
+    launches = dsa.launch_count() - n0
+    s = g.pipe.scores.cpu().numpy()
+    s_ref = oracle_scores(c, ld=s.shape[1])
+    assert_scores_equal(s, s_ref, c.n_elig)
+    idx_ref = oracle.topk(s_ref, c.n_elig, c.K)
+    np.testing.assert_array_equal(g.pipe.idx.cpu().numpy(), idx_ref)
+    out_ref, lse_ref = oracle_attn(c, idx_ref)
+    assert_out_close(g.pipe.out, g.pipe.lse, out_ref, lse_ref, "mixed")
+    assert g.status() == 0
+    assert launches <= 6, launches
+
+
+def test_mixed_batch_rows_do_not_interfere():
+    """Each sequence's rows of a mixed batch equal the rows of that sequence
+    run alone: scores and indices bit for bit, attention within the bar."""
+    need_gpu()
+    lens, nq = (2100, 900, 300), (40, 1, 300)
+    c = _mixed(610, lens, nq, 256)
+    g = GpuRun(c)
+    g.scores_general()
+    s_all = g.pipe.scores.cpu().numpy()
+    idx_all = g.topk().cpu().numpy()
+    out_all, _ = g.attn()
+    out_all = out_all.float().cpu().numpy()
+    start = 0
+    for b, (L, n) in enumerate(zip(lens, nq)):
+        rows = np.arange(start, start + n)
+        start += n
+        solo = W.make_case("solo", seed=610, kind="mixed", seq_lens=lens, q_per_seq=nq, K=256,
+                           **LAT_SHAPES)
+        # the same cache, only sequence b's queries
+        for f in ("q_seq", "q_pos", "n_elig", "q", "q_idx", "w"):
+            setattr(solo, f, getattr(c, f)[rows])
+        gs = GpuRun(solo)
+        gs.scores_general()
+        s = gs.pipe.scores.cpu().numpy()
+        for r in range(n):
+            m = int(c.n_elig[rows[r]])
+            np.testing.assert_array_equal(s[r, :m], s_all[rows[r], :m])
+        np.testing.assert_array_equal(gs.topk().cpu().numpy(), idx_all[rows])
+        o, _ = gs.attn()
+        err = np.abs(o.float().cpu().numpy() - out_all[rows])
+        assert err.max() <= 1e-2, (b, err.max())
+
+
+def test_variable_length_prefill_batch():
+    """Several whole prompts of different lengths (ragged pages) in one batch."""
+    need_gpu()
+    lens = (300, 129, 64, 450, 1)
+    c = _mixed(620, lens, lens, 64)
+    _full_check(c)

@@ -500,3 +500,26 @@ def test_cache_written_at_prefill_serves_the_decode_gather():
                                 Dv=c.Dv)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+def test_mixed_batch_row_equals_decode_of_its_prefix():
+    """A mixed batch (prefill chunk + decode + whole prompt) is row by row the
+    decode of each query's prefix: a query at position t of sequence b sees
+    exactly positions 0..t of b."""
+    c = W.make_case(seed=14, kind="mixed", seq_lens=(90, 40, 33), q_per_seq=(20, 1, 33), bs=16,
+                    Hq=2, Dqk=16, Dv=16, latent=True, H_i=2, D_i=8, idx_dtype="bf16", K=12)
+    assert c.q_seq.tolist() == [0] * 20 + [1] + [2] * 33
+    assert c.q_pos.tolist() == list(range(70, 90)) + [39] + list(range(33))
+    s = scores_of(c)
+    idx = oracle.topk(s, c.n_elig, c.K)
+    out, _ = _attn(c, idx)
+    for r in (0, 19, 20, 21, 53):
+        b, t = int(c.q_seq[r]), int(c.q_pos[r])
+        sl = c.seq_lens.copy()
+        sl[b] = t + 1
+        sd = oracle.index_score(c.block_table, sl, c.bs, c.num_blocks, [b], [t], c.q_idx[r:r + 1],
+                                c.w[r:r + 1], c.kidx_pool, code(c), c.max_len)
+        np.testing.assert_array_equal(sd[0], s[r])
+        od, _ = oracle.sparse_attn(c.block_table, sl, c.bs, c.num_blocks, [b], c.q[r:r + 1],
+                                   c.k_pool, c.v_pool, idx[r:r + 1], c.sm_scale, Dv=c.Dv)
+        np.testing.assert_array_equal(od[0], out[r])

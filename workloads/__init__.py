@@ -96,7 +96,7 @@ class Case:
     """One synthetic problem: paged cache + queries, as host numpy arrays."""
 
     name: str
-    kind: str  # "decode" or "prefill"
+    kind: str  # "decode", "prefill" or "mixed"
     seed: int
     # paged layout
     bs: int
@@ -166,10 +166,13 @@ def make_case(name: str = "custom", *, seed: int = 0, kind: str = "decode",
               Hq: int = 16, Dqk: int = 128, Dv: int = 128, latent: bool = False,
               H_i: int = 4, D_i: int = 64, idx_dtype: str = "bf16", K: int = 256,
               tie_frac: float = 0.0, poison: bool = True, extra_pages: int = 0,
-              q_rows=None) -> Case:
+              q_rows=None, q_per_seq=None) -> Case:
     """Draw one case.  kind="prefill" uses a single sequence of T tokens with one
     query per token (q_pos = t); kind="decode" has one query per sequence at its
-    last position.  q_rows (prefill only) keeps a subset of the T queries."""
+    last position; kind="mixed" gives sequence b the q_per_seq[b] queries at its
+    last positions (1: a decode step, L_b: a whole prompt, in between: a prefill
+    chunk over an existing prefix).  q_rows (prefill only) keeps a subset of the
+    T queries."""
     rng = np.random.Generator(np.random.PCG64(seed))
     if kind == "prefill":
         seq_lens = np.array([T], dtype=np.int32)
@@ -181,6 +184,12 @@ def make_case(name: str = "custom", *, seed: int = 0, kind: str = "decode",
     if kind == "prefill":
         q_pos = np.arange(T, dtype=np.int32) if q_rows is None else np.asarray(q_rows, np.int32)
         q_seq = np.zeros_like(q_pos)
+    elif kind == "mixed":
+        n_q = np.asarray(q_per_seq, dtype=np.int64)
+        assert n_q.shape == (B,) and np.all(n_q >= 1) and np.all(n_q <= seq_lens)
+        q_seq = np.repeat(np.arange(B, dtype=np.int32), n_q)
+        q_pos = np.concatenate([np.arange(int(L) - int(n), int(L), dtype=np.int32)
+                                for L, n in zip(seq_lens, n_q)])
     else:
         q_seq = np.arange(B, dtype=np.int32)
         q_pos = (seq_lens - 1).astype(np.int32)
@@ -215,7 +224,7 @@ def make_case(name: str = "custom", *, seed: int = 0, kind: str = "decode",
             kint[pages[:L // bs]] = vals[:full].reshape(-1, bs, D_i)
             if full < L:
                 kint[pages[-1], :L - full] = vals[full:]
-        if kind == "prefill":
+        if kind != "decode":
             raise ValueError("tie construction is defined for decode cases")
         q_idx = encode_int(qi, idx_dtype)
         kidx_pool = encode_int(kint, idx_dtype)
