@@ -18,9 +18,13 @@
 //   PV  O^T[512 dv x 64 heads] += V^T[512 x 128 rows] . P^T[128 rows x 64]
 //       A = V^T (the first 512 dims of the same rows, MN-major), B = P^T
 //       (MN-major, one 128-byte row per KV row); 4 blocks of 128 dv.
-// P is rounded to bf16 as hi + lo (two PV MMAs) and the softmax denominators
-// sum exactly the values the MMA multiplies, so the only rounding left in the
-// output is the final bf16 store.
+// P is rounded to bf16 once for the PV MMA when the query has more than
+// kSplitRows usable rows; the softmax denominators sum the fp32 values, so
+// each weight of the output's average of V rows is within 2^-9 (relative) of
+// its exact value and lse keeps fp32 accuracy.  A query with fewer rows has a
+// peaked softmax and an output close to a few single V rows, so there P is
+// kept as bf16 hi + lo (two PV MMAs) and the output is exact up to its final
+// bf16 store.
 // The tiles of all queries are laid end to end and split evenly over one CTA
 // per SM.  A query whose tiles span several CTAs leaves one unnormalised
 // partial (O, m, l) per CTA in the workspace and a second small kernel merges
@@ -61,6 +65,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
 constexpr uint32_t kColO = 128;  // four 64-column O^T blocks
 constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kSplitRows = 512;  // queries with at most this many rows: P as hi + lo
 constexpr int kMaxCtas = 160;
 constexpr uint32_t kIdescQK = instr_desc(128, kHq, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
@@ -72,7 +77,7 @@ struct __align__(1024) Smem {
   uint8_t kv[kChunks][kChunkBytes];  // the tile's rows, resident from QK to PV
   uint8_t q[kQRing][kQChunkBytes];   // Q chunks streamed from L2
   uint8_t phi[kPBytes];              // P^T, bf16 part
-  uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi)
+  uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi), short queries only
   uint64_t kfull[kChunks], kempty[kChunks], qfull[kQRing], qempty[kQRing];
   uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done;
   int rowtab[kRows];  // physical rows of the producer's current tile
@@ -88,9 +93,21 @@ struct Geo {
   long long total;
   int G;
   long long lo, hi;
-  __host__ __device__ long long lo_of(int c) const { return (long long)c * total / G; }
+  // 32-bit divisions whenever the products fit (every workload here): a
+  // 64-bit division is a long instruction sequence on the GPU.
+  __host__ __device__ long long lo_of(int c) const {
+    const unsigned long long p = (unsigned long long)c * (unsigned long long)total;
+    if (p < (1ull << 32)) return (long long)((uint32_t)p / (uint32_t)G);
+    return (long long)(p / (unsigned long long)G);
+  }
+  // tile index x -> query index (x / Tq)
+  __host__ __device__ long long query_of(long long x) const {
+    return x < (1ll << 32) ? (long long)((uint32_t)x / (uint32_t)Tq) : x / Tq;
+  }
   __host__ __device__ int cta_of(long long x) const {
-    int c = (int)(x * G / total);
+    const unsigned long long p = (unsigned long long)x * (unsigned long long)G;
+    int c = (p < (1ull << 32) && total < (1ll << 32)) ? (int)((uint32_t)p / (uint32_t)total)
+                                                      : (int)(p / (unsigned long long)total);
     while (c + 1 < G && lo_of(c + 1) <= x) ++c;
     while (c > 0 && lo_of(c) > x) --c;
     return c;
@@ -258,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   g.G = gridDim.x;
   g.lo = g.lo_of(blockIdx.x);
   g.hi = g.lo_of(blockIdx.x + 1);
-  const int r_first = (int)(g.lo / g.Tq);
-  const int r_last = g.hi > g.lo ? (int)((g.hi - 1) / g.Tq) : r_first - 1;
+  const int r_first = (int)g.query_of(g.lo);
+  const int r_last = g.hi > g.lo ? (int)g.query_of(g.hi - 1) : r_first - 1;
   launch_dependents();
 
   if (threadIdx.x == 0) {
@@ -408,15 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first && sa > 1 && !mbar_wait(&sm.ofree, (sa - 2) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        const bool split = w.s.n <= kSplitRows;
         for (int blk = 0; blk < kDv / 128; ++blk) {
           const uint32_t v0 = smem_u32(sm.kv[2 * blk]);  // chunks 2blk, 2blk+1 are 16 KB apart
           const uint32_t d = tbase + kColO + 64 * blk;
+          if (split) {
 #pragma unroll
-          for (int k = 0; k < kRows / 16; ++k) {
-            const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
-            mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
-                    (first && k == 0) ? 0u : 1u);
-            mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
+            for (int k = 0; k < kRows / 16; ++k) {
+              const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
+              mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+                      (first && k == 0) ? 0u : 1u);
+              mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kRows / 16; ++k) {
+              const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
+              mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+                      (first && k == 0) ? 0u : 1u);
+            }
           }
           mma_commit(&sm.kempty[2 * blk]);
           mma_commit(&sm.kempty[2 * blk + 1]);
@@ -519,8 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // pass 2: P = 2^(z - m) as bf16 hi + lo into this row of P^T; the
-        // per-head sums add exactly the values the two PV MMAs multiply
+        // pass 2: P = 2^(z - m) in bf16 (hi + lo for short queries) into this
+        // row of P^T; the per-head sums add the fp32 values
+        const bool split = s.n <= kSplitRows;
         uint8_t* rh = sm.phi + row * 128;
         uint8_t* rl = sm.plo + row * 128;
 #pragma unroll 1
@@ -540,9 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
             const float2 hf = __bfloat1622float2(hi);
             const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-            const float2 lf = __bfloat1622float2(lo);
-            v[i] = hf.x + lf.x;
-            v[i + 1] = hf.y + lf.y;
+            v[i] = p0;
+            v[i + 1] = p1;
             hw[i / 2] = *reinterpret_cast<const uint32_t*>(&hi);
             lw[i / 2] = *reinterpret_cast<const uint32_t*>(&lo);
           }
@@ -551,8 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int off = ((4 * half + k) ^ (row & 7)) << 4;
             *reinterpret_cast<uint4*>(rh + off) =
                 make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-            *reinterpret_cast<uint4*>(rl + off) =
-                make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+            if (split)
+              *reinterpret_cast<uint4*>(rl + off) =
+                  make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
           }
           sm.reds[warp][32 * half + lane] = butterfly32<false>(v, lane);
         }
@@ -627,107 +655,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge of the queries whose tiles span several CTAs.  Grid (8 head groups,
-// G): CTA column c handles the query that contains the boundary lo(c) when c
-// is the first boundary inside that query.
+// Merge of the queries whose tiles span several CTAs.  Grid (16 head groups,
+// Y): with by_query, row y is query y (skipped when it lies inside one CTA);
+// otherwise row y is CTA boundary y + 1, which handles the query containing
+// it when it is the first boundary inside that query.  The first form is
+// used when there are fewer queries than boundaries, so that no block of the
+// grid is idle.  Each thread owns two float4 of dv for one of the group's 4
+// heads and reads, for up to kMergeBatch slots at a time, the slot's (m, l)
+// and its two partial float4 in one go: a query split over at most
+// kMergeBatch CTAs is merged after a single round trip.  Slots beyond the
+// first batch are folded in with a running maximum.
+constexpr int kMergeHeads = 4;
+constexpr int kMergeBatch = 8;
+
 __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, const float* part_o,
-                                                       const float* part_ml) {
+                                                       const float* part_ml, int by_query) {
   grid_dependency_wait();
   launch_dependents();
-  const int c = blockIdx.y + 1;
-  const long long bnd = g.lo_of(c);
-  if (bnd % g.Tq == 0) return;
-  const int r = (int)(bnd / g.Tq);
-  const long long first = (long long)r * g.Tq;
-  if (g.lo_of(c - 1) > first) return;  // an earlier boundary of this query merges it
+  int r;
+  long long first;
+  if (by_query) {
+    r = blockIdx.y;
+    first = (long long)r * g.Tq;
+  } else {
+    const int c = blockIdx.y + 1;
+    const long long bnd = g.lo_of(c);
+    r = (int)g.query_of(bnd);
+    first = (long long)r * g.Tq;
+    if (bnd == first) return;
+    if (g.lo_of(c - 1) > first) return;  // an earlier boundary of this query merges it
+  }
   const int c0 = g.cta_of(first), c1 = g.cta_of(first + g.Tq - 1);
-  const int h0 = blockIdx.x * 8;
-  __shared__ float wgt[8][kMaxCtas + 1], lpart[8][kMaxCtas + 1];
-  __shared__ float lsum[8], mmax[8];
-  __shared__ int pslot[kMaxCtas + 1];
+  if (c1 == c0) return;  // not split: the attention kernel wrote this query
   const int ns = c1 - c0 + 1;
-  // (m, l) of every slot and head of this group, loaded all at once
-  for (int i = threadIdx.x; i < ns * 8; i += blockDim.x) {
-    const int cc = c0 + i / 8, hh = i % 8;
-    const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
-    const float2 ml =
-        __ldcg(reinterpret_cast<const float2*>(part_ml + ((size_t)ps * kHq + h0 + hh) * 2));
-    wgt[hh][i / 8] = ml.y > 0.0f ? ml.x : -INFINITY;
-    lpart[hh][i / 8] = ml.y;
-    if (hh == 0) pslot[i / 8] = ps;
-  }
-  __syncthreads();
-  {
-    // warp hh: M = max m_s, weights 2^(m_s - M), L = sum l_s 2^(m_s - M)
-    const int hh = threadIdx.x >> 5, ln = threadIdx.x & 31;
-    float M = -INFINITY;
-    for (int j = ln; j < ns; j += 32) M = fmaxf(M, wgt[hh][j]);
-    M = warp_max(M);
-    float L = 0.0f;
-    for (int j = ln; j < ns; j += 32) {
-      const float mj = wgt[hh][j];
-      const float w = mj > -INFINITY ? exp2f(mj - M) : 0.0f;
-      L += lpart[hh][j] * w;
-      wgt[hh][j] = w;
+  const int h = blockIdx.x * kMergeHeads + (threadIdx.x >> 6);  // 64 threads per head
+  const int q4 = threadIdx.x & 63;                               // float4 q4 and q4 + 64 of dv
+  float M = -INFINITY, L = 0.0f;
+  float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+  for (int j0 = 0; j0 < ns; j0 += kMergeBatch) {
+    const int nb = min(kMergeBatch, ns - j0);
+    float2 ml[kMergeBatch];
+    float4 v0[kMergeBatch], v1[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (j < nb) {
+        const int cc = c0 + j0 + j;
+        const int ps = 2 * cc + ((first > g.lo_of(cc)) ? 1 : 0);
+        ml[j] = __ldcg(reinterpret_cast<const float2*>(part_ml + ((size_t)ps * kHq + h) * 2));
+        const float4* src =
+            reinterpret_cast<const float4*>(part_o + ((size_t)ps * kHq + h) * kDv) + q4;
+        v0[j] = __ldcg(src);
+        v1[j] = __ldcg(src + 64);
+      }
     }
-    L = warp_sum(L);
-    if (ln == 0) {
-      lsum[hh] = L;
-      mmax[hh] = M;
+    float Mb = M;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (j < nb && ml[j].y > 0.0f) Mb = fmaxf(Mb, ml[j].x);
+    if (Mb == -INFINITY) continue;
+    const float f = M > -INFINITY ? exp2f(M - Mb) : 0.0f;
+    L *= f;
+    acc0.x *= f; acc0.y *= f; acc0.z *= f; acc0.w *= f;
+    acc1.x *= f; acc1.y *= f; acc1.z *= f; acc1.w *= f;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (j < nb && ml[j].y > 0.0f) {
+        const float w = exp2f(ml[j].x - Mb);
+        L = fmaf(ml[j].y, w, L);
+        acc0.x = fmaf(w, v0[j].x, acc0.x); acc0.y = fmaf(w, v0[j].y, acc0.y);
+        acc0.z = fmaf(w, v0[j].z, acc0.z); acc0.w = fmaf(w, v0[j].w, acc0.w);
+        acc1.x = fmaf(w, v1[j].x, acc1.x); acc1.y = fmaf(w, v1[j].y, acc1.y);
+        acc1.z = fmaf(w, v1[j].z, acc1.z); acc1.w = fmaf(w, v1[j].w, acc1.w);
+      }
     }
+    M = Mb;
   }
-  __syncthreads();
-  // thread t owns outputs t + 256 k (k < 16): head k/2, dv t + 256 (k & 1);
-  // slots are taken two at a time, so 32 independent loads are in flight
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-  int j = 0;
-  for (; j + 1 < ns; j += 2) {
-    const float* s0 = part_o + ((size_t)pslot[j] * kHq + h0) * kDv + threadIdx.x;
-    const float* s1 = part_o + ((size_t)pslot[j + 1] * kHq + h0) * kDv + threadIdx.x;
-    float v0[16], v1[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      v0[k] = __ldcg(s0 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
-      v1[k] = __ldcg(s1 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float w0 = wgt[k >> 1][j], w1 = wgt[k >> 1][j + 1];
-      acc[k] = w0 > 0.0f ? fmaf(w0, v0[k], acc[k]) : acc[k];
-      acc[k] = w1 > 0.0f ? fmaf(w1, v1[k], acc[k]) : acc[k];
-    }
-  }
-  if (j < ns) {
-    const float* s0 = part_o + ((size_t)pslot[j] * kHq + h0) * kDv + threadIdx.x;
-    float v0[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) v0[k] = __ldcg(s0 + (size_t)(k >> 1) * kDv + 256 * (k & 1));
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float w0 = wgt[k >> 1][j];
-      acc[k] = w0 > 0.0f ? fmaf(w0, v0[k], acc[k]) : acc[k];
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int hh = k >> 1, dv = threadIdx.x + 256 * (k & 1);
-    const float L = lsum[hh];
-    a.out[((size_t)r * kHq + h0 + hh) * kDv + dv] = __float2bfloat16(L > 0.0f ? acc[k] / L : 0.0f);
-  }
-  if (a.lse && threadIdx.x < 8) {
-    const float L = lsum[threadIdx.x];
-    a.lse[(size_t)r * kHq + h0 + threadIdx.x] =
-        L > 0.0f ? (mmax[threadIdx.x] + log2f(L)) * 0.6931471805599453f : -INFINITY;
-  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  __nv_bfloat16* o = a.out + ((size_t)r * kHq + h) * kDv + 4 * q4;
+  __nv_bfloat162 p[4] = {__floats2bfloat162_rn(acc0.x * inv, acc0.y * inv),
+                         __floats2bfloat162_rn(acc0.z * inv, acc0.w * inv),
+                         __floats2bfloat162_rn(acc1.x * inv, acc1.y * inv),
+                         __floats2bfloat162_rn(acc1.z * inv, acc1.w * inv)};
+  *reinterpret_cast<uint2*>(o) = make_uint2(*reinterpret_cast<uint32_t*>(&p[0]),
+                                            *reinterpret_cast<uint32_t*>(&p[1]));
+  *reinterpret_cast<uint2*>(o + 256) = make_uint2(*reinterpret_cast<uint32_t*>(&p[2]),
+                                                  *reinterpret_cast<uint32_t*>(&p[3]));
+  if (a.lse && q4 == 0)
+    a.lse[(size_t)r * kHq + h] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 }  // namespace
 
 bool attn_tc_eligible(const AttnParams& p) {
+  // the merge stores four bf16 at a time: out must be 8-byte aligned
   return p.Hq == kHq && p.Dqk == kDqk && p.Dv == kDv && p.kp == p.vp && p.ks == kDqk &&
-         p.vs == kDqk && p.Nq >= 1 &&
+         p.vs == kDqk && p.Nq >= 1 && ((uintptr_t)p.out & 7u) == 0 &&
          (long long)p.lay.nb * p.lay.bs < (1LL << 31) - 1;
 }
 
@@ -761,8 +783,10 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   rc = check_launch("sparse_attn (tensor cores)");
   if (rc || grid < 2) return rc;
-  e = launch_pdl(k_attn_tc_merge, dim3(kHq / 8, (unsigned)(grid - 1)), dim3(256), 0, s, p, g,
-                 (const float*)part_o, (const float*)part_ml);
+  const int by_query = p.Nq <= grid - 1 ? 1 : 0;
+  e = launch_pdl(k_attn_tc_merge,
+                 dim3(kHq / kMergeHeads, (unsigned)(by_query ? p.Nq : grid - 1)), dim3(256), 0, s,
+                 p, g, (const float*)part_o, (const float*)part_ml, by_query);
   count_launch();
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("sparse_attn merge");
