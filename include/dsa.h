@@ -248,8 +248,11 @@ int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const
  * physical row block_table[seq][pos / block_size] * block_size
  * + pos % block_size -- the same mapping every gather above uses.
  *
- *  layout      paged layout (seq_lens is not read: the caller owns lengths)
- *  seq, pos    [N] int32 sequence and position of each new row
+ *  layout      paged layout (seq_lens is read only by the append form)
+ *  seq, pos    [N] int32 sequence and position of each new row; both NULL:
+ *              the append form of a decode step, row i goes to position
+ *              seq_lens[i] - 1 of sequence i (N <= batch; seq_lens already
+ *              counts the new token)
  *  kv_new      [N][row_elems] bf16 rows (K, or the latent K/V row), or NULL
  *  row_elems   bf16 elements per row, a multiple of 8
  *  kv_pool     physical rows of row_elems bf16, kv_row_stride elements apart
@@ -269,6 +272,54 @@ int dsa_cache_write(const dsa_paged_layout* layout, const int32_t* seq, const in
                     const void* kv_new, int row_elems, void* kv_pool, int64_t kv_row_stride,
                     const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, void* ws,
                     size_t ws_bytes, dsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole steps: one call for one decode step or one prefill (chunk), each the
+ * cache write followed by the three stages on `stream` (no host
+ * synchronisation in between).  Source: "Day-0 Adaptation of
+ * Trillion-Parameter MoE Models on Domestic GPUs", section 3 (3): decode
+ * indexing is incremental -- the indexer keys of earlier positions stay in
+ * the cache and a step only adds the new position's row before scoring --
+ * and prefill handles a whole prompt at once; "Day-0 Adaptation of
+ * Ultra-Large-Scale MoE Models on Heterogeneous AI Accelerators", section 4:
+ * index selection, KV cache write, then gather + sparse attention.
+ *
+ * dsa_decode_step: layout->seq_lens[b] already counts sequence b's new token.
+ *  k_new       [B][Dqk] bf16 new K rows (the latent row for a latent cache),
+ *              written at position seq_lens[b] - 1 of k_pool (rows
+ *              k_row_stride elements apart)
+ *  v_new       [B][Dv] bf16 new V rows into v_pool, or NULL when v_pool is
+ *              k_pool and V is the first Dv dims of the K row
+ *  kidx_new    [B][D_i] new indexer-key rows of idx_dtype into kidx_pool
+ *  q_idx, w, q as for dsa_index_score / dsa_sparse_attn_decode (query b is
+ *              sequence b at its newest position)
+ *  scores      [B][ld], idx [B][K], out [B][Hq][Dv], lse [B][Hq] or NULL
+ *  ws          dsa_decode_step_workspace_size(...) bytes; the step's status
+ *              word (all stages OR into it) is at offset 0
+ * dsa_prefill_step: the Nq queries of sequence `seq` at positions q_pos
+ * (device [Nq]); their new rows (k_new/v_new/kidx_new, [Nq][...]) are written
+ * at those positions first, so a prompt (or a chunk of one after an existing
+ * prefix) is cached and attended in one call; n_eligible [Nq] = q_pos + 1.
+ * Errors: those of the calls the step makes, with nothing after the first
+ * failing call launched.
+ */
+size_t dsa_decode_step_workspace_size(int B, int H_i, int D_i, int64_t ld, int Hq, int Dqk,
+                                      int Dv, int K);
+int dsa_decode_step(const dsa_paged_layout* layout, const void* k_new, void* k_pool,
+                    int64_t k_row_stride, const void* v_new, void* v_pool, int64_t v_row_stride,
+                    const void* kidx_new, void* kidx_pool, int idx_dtype, const void* q_idx,
+                    const float* w, int H_i, int D_i, const void* q, int Hq, int Dqk, int Dv,
+                    int K, float sm_scale, float* scores, int64_t ld, int32_t* idx, void* out,
+                    float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream);
+size_t dsa_prefill_step_workspace_size(int Nq, int H_i, int D_i, int64_t ld, int Hq, int Dqk,
+                                       int Dv, int K);
+int dsa_prefill_step(const dsa_paged_layout* layout, int seq, const int32_t* q_pos,
+                     const int32_t* n_eligible, int Nq, const void* k_new, void* k_pool,
+                     int64_t k_row_stride, const void* v_new, void* v_pool, int64_t v_row_stride,
+                     const void* kidx_new, void* kidx_pool, int idx_dtype, const void* q_idx,
+                     const float* w, int H_i, int D_i, const void* q, int Hq, int Dqk, int Dv,
+                     int K, float sm_scale, float* scores, int64_t ld, int32_t* idx, void* out,
+                     float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Utilities (no counterpart on the pages).

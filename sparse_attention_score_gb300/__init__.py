@@ -85,6 +85,13 @@ _sig("dsa_index_score_prefill", _i, [_LP, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _i
 _sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
 _sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_topk_noalloc", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp])
+_sig("dsa_decode_step_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, _i, _i])
+_sig("dsa_decode_step", _i, [_LP, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i, _vp, _vp, _i, _i,
+                             _vp, _i, _i, _i, _i, _f, _vp, _i64, _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("dsa_prefill_step_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, _i, _i])
+_sig("dsa_prefill_step", _i, [_LP, _i, _vp, _vp, _i, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i,
+                              _vp, _vp, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _i64, _vp, _vp, _vp,
+                              _vp, _sz, _vp])
 _sig("dsa_cache_write_workspace_size", _sz, [])
 _sig("dsa_cache_write", _i, [_LP, _vp, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
@@ -100,7 +107,9 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_topk_workspace_size",
            "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
            "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill",
-           "dsa_cache_write_workspace_size", "dsa_cache_write")
+           "dsa_cache_write_workspace_size", "dsa_cache_write",
+           "dsa_decode_step_workspace_size", "dsa_decode_step",
+           "dsa_prefill_step_workspace_size", "dsa_prefill_step")
 
 
 def lib() -> ctypes.CDLL:
@@ -271,6 +280,50 @@ def cache_write(layout: PagedLayout, seq, pos, ws, kv_new=None, kv_pool=None, ki
                               _ptr(kv_pool), stride, _ptr(kidx_new), D_i, kdt, _ptr(kidx_pool),
                               _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "dsa_cache_write")
+
+
+def decode_step_workspace_size(B, H_i, D_i, ld, Hq, Dqk, Dv, K) -> int:
+    return int(_lib.dsa_decode_step_workspace_size(B, H_i, D_i, ld, Hq, Dqk, Dv, K))
+
+
+def prefill_step_workspace_size(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K) -> int:
+    return int(_lib.dsa_prefill_step_workspace_size(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K))
+
+
+def decode_step(layout: PagedLayout, k_new, k_pool, kidx_new, kidx_pool, q_idx, w, q, K, sm_scale,
+                scores, idx, out, lse, ws, v_new=None, v_pool=None, stream=None):
+    """One incremental decode step (include/dsa.h, dsa_decode_step): append each
+    sequence's new K/V and indexer-key rows at position seq_lens[b] - 1, then
+    score, select and attend.  v_pool None: V is the first Dv dims of the K row."""
+    B, Hq, Dqk = q.shape
+    H_i, D_i = q_idx.shape[1], q_idx.shape[2]
+    vp = k_pool if v_pool is None else v_pool
+    rc = _lib.dsa_decode_step(layout.c(), _ptr(k_new), _ptr(k_pool), k_pool.shape[-1], _ptr(v_new),
+                              _ptr(vp), vp.shape[-1], _ptr(kidx_new), _ptr(kidx_pool),
+                              _elt_dtype(kidx_pool), _ptr(q_idx), _ptr(w), H_i, D_i, _ptr(q), Hq,
+                              Dqk, out.shape[2], int(K), float(sm_scale), _ptr(scores),
+                              scores.shape[1], _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
+                              ws.numel(), _stream(stream))
+    _check(rc, "dsa_decode_step")
+
+
+def prefill_step(layout: PagedLayout, seq, q_pos, n_eligible, k_new, k_pool, kidx_new, kidx_pool,
+                 q_idx, w, q, K, sm_scale, scores, idx, out, lse, ws, v_new=None, v_pool=None,
+                 stream=None):
+    """A prompt (or a chunk after an existing prefix) of sequence `seq` in one
+    call (include/dsa.h, dsa_prefill_step): its rows are written at q_pos, then
+    scored, selected and attended."""
+    Nq, Hq, Dqk = q.shape
+    H_i, D_i = q_idx.shape[1], q_idx.shape[2]
+    vp = k_pool if v_pool is None else v_pool
+    rc = _lib.dsa_prefill_step(layout.c(), int(seq), _ptr(q_pos), _ptr(n_eligible), Nq,
+                               _ptr(k_new), _ptr(k_pool), k_pool.shape[-1], _ptr(v_new), _ptr(vp),
+                               vp.shape[-1], _ptr(kidx_new), _ptr(kidx_pool),
+                               _elt_dtype(kidx_pool), _ptr(q_idx), _ptr(w), H_i, D_i, _ptr(q), Hq,
+                               Dqk, out.shape[2], int(K), float(sm_scale), _ptr(scores),
+                               scores.shape[1], _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
+                               ws.numel(), _stream(stream))
+    _check(rc, "dsa_prefill_step")
 
 
 def get_status(ws, clear: bool = True, stream=None) -> int:

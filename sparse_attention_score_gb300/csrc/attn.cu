@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
 
   const int r = blockIdx.y, split = blockIdx.x, S = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = a.q_seq ? __ldg(&a.q_seq[r]) : (a.seq0 ? 0 : r);
+  const int b = a.q_seq ? __ldg(&a.q_seq[r]) : (a.seq_const >= 0 ? a.seq_const : r);
   const bool b_ok = b >= 0 && b < a.lay.batch;
 
   for (int i = threadIdx.x; i < Hq * Dqk / 8; i += kAttnThreads)

@@ -133,7 +133,7 @@ __device__ __forceinline__ Seg make_seg(const AttnParams& a, const Geo& g, int r
   s.t0 = (int)(g.lo > base ? g.lo - base : 0);
   s.t1 = (int)min((long long)g.Tq, g.hi - base);
   s.complete = (s.t0 == 0 && s.t1 == g.Tq);
-  s.b = a.q_seq ? __ldg(&a.q_seq[r]) : (a.seq0 ? 0 : r);
+  s.b = a.q_seq ? __ldg(&a.q_seq[r]) : (a.seq_const >= 0 ? a.seq_const : r);
   s.n = 0;
   s.L = 0;
   s.qp = -1;

@@ -36,6 +36,7 @@ struct CacheWriteParams {
   uint4* kidx_pool;
   int kidx_g;
   int* status;
+  int seq_const;  // seq NULL with pos given: every row in this sequence
 };
 
 // Granules a lane holds in registers (rows up to 32 * kHeld granules, i.e.
@@ -52,8 +53,13 @@ __global__ void __launch_bounds__(kWarps * 32, 5) k_cache_write(CacheWriteParams
   const long long gw = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const long long nw = (long long)gridDim.x * kWarps;
   for (long long i = gw; i < p.N; i += nw) {
-    const int b = __ldg(&p.seq[i]);
-    const long long ps = __ldg(&p.pos[i]);
+    // append form (seq / pos NULL): row i is the newest position of sequence i
+    const int b = p.seq ? __ldg(&p.seq[i]) : (p.pos ? p.seq_const : (int)i);
+    long long ps = -1;
+    if (p.pos)
+      ps = __ldg(&p.pos[i]);
+    else if (b >= 0 && b < p.lay.batch)
+      ps = (long long)__ldg(&p.lay.seq_lens[b]) - 1;
     uint4 v[kHeld];
     uint4 vi = make_uint4(0, 0, 0, 0);
     const uint4* src = p.kv_new ? p.kv_new + i * p.kv_g : nullptr;
@@ -94,10 +100,13 @@ bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
 int cache_write(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, int N,
                 const void* kv_new, int row_elems, void* kv_pool, long long kv_row_stride,
                 const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, int* status,
-                cudaStream_t s) {
+                cudaStream_t s, int seq_const) {
   if (N < 0) return set_error(DSA_ERR_INVALID, "cache_write: N < 0");
   if (N == 0) return DSA_OK;
-  if (!seq || !pos) return set_error(DSA_ERR_INVALID, "cache_write: seq / pos is NULL");
+  if ((seq == nullptr) != (pos == nullptr) && !(seq == nullptr && seq_const >= 0))
+    return set_error(DSA_ERR_INVALID, "cache_write: give both seq and pos, or neither (append)");
+  if (!seq && !pos && N > lay.batch)
+    return set_error(DSA_ERR_INVALID, "cache_write: append form needs N <= batch");
   if (!kv_new && !kidx_new) return set_error(DSA_ERR_INVALID, "cache_write: nothing to write");
   CacheWriteParams p{};
   p.lay = lay;
@@ -105,6 +114,7 @@ int cache_write(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, in
   p.pos = pos;
   p.N = N;
   p.status = status;
+  p.seq_const = seq_const;
   if (kv_new) {
     if (!kv_pool) return set_error(DSA_ERR_INVALID, "cache_write: kv_pool is NULL");
     if (row_elems < 8 || row_elems % 8 || kv_row_stride < row_elems || kv_row_stride % 8)

@@ -95,7 +95,7 @@ static int index_common(const dsa_paged_layout* layout, const void* q_idx, const
                         const void* kidx_pool, int dtype, int H_i, int D_i,
                         const int32_t* q_seq, const int32_t* q_pos, int seq_const, int Nq,
                         float* scores, int64_t ld, void* ws, size_t ws_bytes,
-                        dsa_stream_t stream) {
+                        dsa_stream_t stream, int* status = nullptr) {
   IndexParams p{};
   int rc = check_layout(layout, &p.lay);
   if (rc) return rc;
@@ -123,7 +123,7 @@ static int index_common(const dsa_paged_layout* layout, const void* q_idx, const
   p.Nq = Nq;
   p.scores = scores;
   p.ld = (long long)ld;
-  p.status = reinterpret_cast<int*>(ws);
+  p.status = status ? status : reinterpret_cast<int*>(ws);
   return launch_index_score(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -152,8 +152,9 @@ size_t dsa_topk_workspace_size(int Nq, int64_t ld, int K) {
   return topk_ws(Nq, (long long)ld, K);
 }
 
-int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
-             int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+static int topk_common(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
+                       int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream,
+                       int* status = nullptr) {
   if (Nq < 0 || ld < 1 || K < 1 || K > 65536)
     return set_error(DSA_ERR_INVALID, "topk: need Nq >= 0, ld >= 1, 1 <= K <= 65536");
   if (!scores || !n_eligible || !idx) return set_error(DSA_ERR_INVALID, "topk: NULL pointer");
@@ -166,8 +167,13 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
   p.Nq = Nq;
   p.K = K;
   p.idx = idx;
-  p.status = reinterpret_cast<int*>(ws);
+  p.status = status ? status : reinterpret_cast<int*>(ws);
   return launch_topk(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
+             int32_t* idx, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  return topk_common(scores, ld, n_eligible, Nq, K, idx, ws, ws_bytes, stream);
 }
 
 size_t dsa_cache_write_workspace_size(void) { return kWsHeader; }
@@ -191,7 +197,8 @@ static int attn_common(const dsa_paged_layout* layout, const void* q, const void
                        int Dqk, int Dv, const int32_t* q_seq, const int32_t* q_pos, int Nq,
                        const int32_t* idx, int K,
                        float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
-                       dsa_stream_t stream, bool decode) {
+                       dsa_stream_t stream, bool decode, int* status = nullptr,
+                       int seq_const = -2) {
   AttnParams p{};
   int rc = check_layout(layout, &p.lay);
   if (rc) return rc;
@@ -221,14 +228,14 @@ static int attn_common(const dsa_paged_layout* layout, const void* q, const void
   p.Dv = Dv;
   p.q_seq = q_seq;
   p.q_pos = q_pos;
-  p.seq0 = decode ? 0 : 1;
+  p.seq_const = seq_const >= -1 ? seq_const : (decode ? -1 : 0);
   p.Nq = Nq;
   p.idx = idx;
   p.K = K;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.status = reinterpret_cast<int*>(ws);
+  p.status = status ? status : reinterpret_cast<int*>(ws);
   return launch_attn(p, decode, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -258,6 +265,116 @@ int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const
                             dsa_stream_t stream) {
   return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, q_seq,
                      q_pos, Nq, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, false);
+}
+
+// ---------------------------------------------------------------- steps --
+// A step workspace: the step's status header, then one region per stage
+// (each region 256-byte aligned and laid out as that stage's own workspace).
+// Every stage ORs its status bits into the step's word at offset 0.
+static size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+struct StepLayout {
+  size_t off_index, off_topk, off_attn, total;
+};
+
+static StepLayout step_layout(int Nq, int H_i, int D_i, int64_t ld, int Hq, int Dqk, int Dv, int K,
+                              bool decode) {
+  StepLayout L;
+  L.off_index = kWsHeader;
+  L.off_topk = L.off_index + round256(index_score_ws(Nq, H_i, D_i, (long long)ld));
+  L.off_attn = L.off_topk + round256(topk_ws(Nq, (long long)ld, K));
+  L.total = L.off_attn + round256(attn_ws(Nq, Hq, Dqk, Dv, K, decode));
+  return L;
+}
+
+static int step_cache_write(const dsa_paged_layout* layout, int seq_const, const int32_t* pos,
+                            int N, const void* k_new, void* k_pool, int64_t k_row_stride, int Dqk,
+                            const void* v_new, void* v_pool, int64_t v_row_stride, int Dv,
+                            const void* kidx_new, void* kidx_pool, int idx_dtype, int D_i,
+                            int* status, cudaStream_t s) {
+  LayoutDev lay;
+  int rc = check_layout(layout, &lay);
+  if (rc) return rc;
+  if (k_new || kidx_new) {
+    rc = cache_write(lay, nullptr, pos, N, k_new, Dqk, k_pool, (long long)k_row_stride, kidx_new,
+                     D_i, idx_dtype, kidx_pool, status, s, seq_const);
+    if (rc) return rc;
+  }
+  if (v_new)
+    rc = cache_write(lay, nullptr, pos, N, v_new, Dv, v_pool, (long long)v_row_stride, nullptr, 0,
+                     0, nullptr, status, s, seq_const);
+  return rc;
+}
+
+size_t dsa_decode_step_workspace_size(int B, int H_i, int D_i, int64_t ld, int Hq, int Dqk,
+                                      int Dv, int K) {
+  return step_layout(B, H_i, D_i, ld, Hq, Dqk, Dv, K, true).total;
+}
+
+int dsa_decode_step(const dsa_paged_layout* layout, const void* k_new, void* k_pool,
+                    int64_t k_row_stride, const void* v_new, void* v_pool, int64_t v_row_stride,
+                    const void* kidx_new, void* kidx_pool, int idx_dtype, const void* q_idx,
+                    const float* w, int H_i, int D_i, const void* q, int Hq, int Dqk, int Dv,
+                    int K, float sm_scale, float* scores, int64_t ld, int32_t* idx, void* out,
+                    float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (!layout) return set_error(DSA_ERR_INVALID, "decode_step: NULL layout");
+  const int B = layout->batch;
+  const StepLayout L = step_layout(B, H_i, D_i, ld, Hq, Dqk, Dv, K, true);
+  int rc = check_ws(ws, ws_bytes, L.total);
+  if (rc) return rc;
+  char* base = reinterpret_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = step_cache_write(layout, -1, nullptr, B, k_new, k_pool, k_row_stride, Dqk, v_new, v_pool,
+                        v_row_stride, Dv, kidx_new, kidx_pool, idx_dtype, D_i, status, s);
+  if (rc) return rc;
+  rc = index_common(layout, q_idx, w, kidx_pool, idx_dtype, H_i, D_i, nullptr, nullptr, -1, B,
+                    scores, ld, base + L.off_index, L.off_topk - L.off_index, stream, status);
+  if (rc) return rc;
+  rc = topk_common(scores, ld, layout->seq_lens, B, K, idx, base + L.off_topk,
+                   L.off_attn - L.off_topk, stream, status);
+  if (rc) return rc;
+  return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, nullptr,
+                     nullptr, B, idx, K, sm_scale, out, lse, base + L.off_attn,
+                     L.total - L.off_attn, stream, true, status);
+}
+
+size_t dsa_prefill_step_workspace_size(int Nq, int H_i, int D_i, int64_t ld, int Hq, int Dqk,
+                                       int Dv, int K) {
+  return step_layout(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K, false).total;
+}
+
+int dsa_prefill_step(const dsa_paged_layout* layout, int seq, const int32_t* q_pos,
+                     const int32_t* n_eligible, int Nq, const void* k_new,
+                     void* k_pool, int64_t k_row_stride, const void* v_new, void* v_pool,
+                     int64_t v_row_stride, const void* kidx_new, void* kidx_pool, int idx_dtype,
+                     const void* q_idx, const float* w, int H_i, int D_i, const void* q, int Hq,
+                     int Dqk, int Dv, int K, float sm_scale, float* scores, int64_t ld,
+                     int32_t* idx, void* out, float* lse, void* ws, size_t ws_bytes,
+                     dsa_stream_t stream) {
+  if (!layout) return set_error(DSA_ERR_INVALID, "prefill_step: NULL layout");
+  if (seq < 0 || seq >= layout->batch)
+    return set_error(DSA_ERR_INVALID, "prefill_step: seq out of range");
+  if (!q_pos || !n_eligible)
+    return set_error(DSA_ERR_INVALID, "prefill_step: q_pos and n_eligible are required");
+  const StepLayout L = step_layout(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K, false);
+  int rc = check_ws(ws, ws_bytes, L.total);
+  if (rc) return rc;
+  char* base = reinterpret_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = step_cache_write(layout, seq, q_pos, Nq, k_new, k_pool, k_row_stride, Dqk, v_new, v_pool,
+                        v_row_stride, Dv, kidx_new, kidx_pool, idx_dtype, D_i, status, s);
+  if (rc) return rc;
+  rc = index_common(layout, q_idx, w, kidx_pool, idx_dtype, H_i, D_i, nullptr, q_pos, seq, Nq,
+                    scores, ld, base + L.off_index, L.off_topk - L.off_index, stream, status);
+  if (rc) return rc;
+  rc = topk_common(scores, ld, n_eligible, Nq, K, idx, base + L.off_topk,
+                   L.off_attn - L.off_topk, stream, status);
+  if (rc) return rc;
+  return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, nullptr,
+                     q_pos, Nq, idx, K, sm_scale, out, lse, base + L.off_attn,
+                     L.total - L.off_attn, stream, false, status, seq);
 }
 
 }  // extern "C"

@@ -57,7 +57,7 @@ struct AttnParams {
   long long vs;
   int Hq, Dqk, Dv;
   const int32_t* q_seq;  // NULL: query r is sequence r (decode) / sequence 0 (prefill)
-  int seq0;              // 1: q_seq NULL means every query is in sequence 0
+  int seq_const;         // q_seq NULL: every query in this sequence (>= 0), or query r in sequence r (-1)
   const int32_t* q_pos;  // NULL or [Nq]: causal bound of each query (prefill)
   int Nq;
   const int32_t* idx;
@@ -93,7 +93,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 int cache_write(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, int N,
                 const void* kv_new, int row_elems, void* kv_pool, long long kv_row_stride,
                 const void* kidx_new, int D_i, int kidx_dtype, void* kidx_pool, int* status,
-                cudaStream_t s);
+                cudaStream_t s, int seq_const = -1);
 
 // host-side bookkeeping (dsa_api.cu)
 void count_launch(int n = 1);

@@ -8,8 +8,13 @@ from workloads import device as wdev
 
 # Tolerances on attention outputs against the fp64 oracle (bf16 I/O, fp32
 # accumulation): max-abs 1e-2 and mean-abs 2e-3 on out; lse to 1e-3 absolute.
+# The output is stored as bf16, whose rounding alone moves a value by up to
+# 2^-9 of its magnitude (more than 1e-2 once |out| > 5.12, which a query with
+# a few selected rows reaches), so the max-abs bar applies to the error left
+# after that rounding: |gpu - ref| <= 1e-2 + 2^-9 |ref|.
 OUT_MAX_ABS = 1e-2
 OUT_MEAN_ABS = 2e-3
+BF16_HALF_ULP_REL = 2.0 ** -9
 LSE_ABS = 1e-3
 
 
@@ -115,7 +120,9 @@ def assert_out_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     err = np.abs(o - out_ref)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
-    assert err.max() <= OUT_MAX_ABS, f"{what}: max-abs {err.max():.3e}"
+    excess = err - BF16_HALF_ULP_REL * np.abs(out_ref)
+    assert excess.max() <= OUT_MAX_ABS, (
+        f"{what}: max-abs {err.max():.3e} ({excess.max():.3e} beyond the bf16 store's rounding)")
     assert err.mean() <= OUT_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
     if lse_gpu is not None:
         l = lse_gpu.cpu().numpy().astype(np.float64)
@@ -145,3 +152,34 @@ def check_topk_definition(s, n, K, idx):
     wk = np.lexsort((-kept, ks))[0]
     bd = np.lexsort((dp, -ds))[0]
     assert ks[wk] > ds[bd] or (ks[wk] == ds[bd] and kept[wk] < dp[bd])
+
+
+# ------------------------------------------------ host <-> device marshalling --
+def logical_rows(case, pool, b, L):
+    """Rows 0..L-1 of sequence b read through the case's block table."""
+    pages = case.block_table[b, :(L + case.bs - 1) // case.bs]
+    return pool[pages].reshape(-1, pool.shape[-1])[:L]
+
+
+def to_dev(a):
+    """Host array -> device tensor of the same bytes (uint16 -> bf16 view)."""
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.cuda()
+
+
+def to_host(t, like):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy().astype(like.dtype, copy=False)
+
+
+def fresh_layout(case, seed, extra):
+    """Another page assignment for the same sequences, with spare pages."""
+    nb2 = case.num_blocks + extra
+    perm = np.random.default_rng(seed).permutation(nb2).astype(np.int32)
+    bt2 = np.full_like(case.block_table, -1)
+    used = case.block_table >= 0
+    bt2[used] = perm[:int(used.sum())]
+    return bt2, nb2

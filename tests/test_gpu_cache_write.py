@@ -13,8 +13,8 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import (GpuRun, assert_out_close, assert_scores_equal, lib, need_gpu, oracle_attn,
-                        oracle_scores)
+from gpu_common import (GpuRun, assert_out_close, assert_scores_equal, fresh_layout, lib,
+                        logical_rows, need_gpu, oracle_attn, oracle_scores, to_dev, to_host)
 from workloads import device as wdev
 
 pytestmark = pytest.mark.gpu
@@ -23,33 +23,10 @@ LAT_SHAPES = dict(Hq=64, Dqk=576, Dv=512, latent=True, H_i=64, D_i=128, idx_dtyp
 TINY_SHAPES = dict(Hq=16, Dqk=128, Dv=128, latent=False, H_i=4, D_i=64, idx_dtype="bf16")
 
 
-def _logical(case, pool, b, L):
-    pages = case.block_table[b, :(L + case.bs - 1) // case.bs]
-    return pool[pages].reshape(-1, pool.shape[-1])[:L]
-
-
-def _dev(a):
-    """Host array -> device tensor of the same bytes (uint16 -> bf16 view)."""
-    t = torch.from_numpy(np.ascontiguousarray(a))
-    if a.dtype == np.uint16:
-        t = t.view(torch.int16).view(torch.bfloat16)
-    return t.cuda()
-
-
-def _host(t, like):
-    if t.dtype == torch.bfloat16:
-        return t.view(torch.int16).cpu().numpy().view(np.uint16)
-    return t.cpu().numpy().astype(like.dtype, copy=False)
-
-
-def _fresh_layout(case, seed, extra):
-    """Another page assignment for the same sequences, with spare pages."""
-    nb2 = case.num_blocks + extra
-    perm = np.random.default_rng(seed).permutation(nb2).astype(np.int32)
-    bt2 = np.full_like(case.block_table, -1)
-    used = case.block_table >= 0
-    bt2[used] = perm[:int(used.sum())]
-    return bt2, nb2
+_logical = logical_rows
+_dev = to_dev
+_host = to_host
+_fresh_layout = fresh_layout
 
 
 def _write(dsa, layout, seq, pos, kv_rows, kv_pool, ki_rows, ki_pool, ws):

@@ -373,7 +373,7 @@ def test_mixed_batch_rows_do_not_interfere():
         np.testing.assert_array_equal(gs.topk().cpu().numpy(), idx_all[rows])
         o, _ = gs.attn()
         err = np.abs(o.float().cpu().numpy() - out_all[rows])
-        assert err.max() <= 1e-2, (b, err.max())
+        assert err.max() <= 1e-2 + 2.0 ** -9 * np.abs(out_all[rows]).max(), (b, err.max())
 
 
 def test_variable_length_prefill_batch():
