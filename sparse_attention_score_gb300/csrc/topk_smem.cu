@@ -31,37 +31,41 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 49152;  // keys per CTA in shared memory (192 KB)
 
+constexpr int kWords = kCap / 32;  // one bit per key
+
 struct Shared {
   int hist[2048];
-  int scan[kWarps + 1];
+  uint32_t gtm[kWords], eqm[kWords];  // per 32 keys: which are > T, which == T
+  uint32_t scan[kWarps + 1];
   int wgt[kWarps], weq[kWarps];
   int sel_bin, sel_above;
   int chunk_off[33];
 };
 
-// Inclusive block scan of one int per thread; returns the inclusive value.
-__device__ __forceinline__ int block_incl_scan(int v, int* sh) {
+// Inclusive block scan of one unsigned value per thread (sums wrap modulo
+// 2^32, which packed counts rely on); returns the inclusive value.
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  uint32_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
   if (lane == 31) sh[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int w = sh[lane];
-    int wi = w;
+    const uint32_t w = sh[lane];
+    uint32_t wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += t;
     }
     sh[lane] = wi - w;  // exclusive prefix of warp totals
   }
   __syncthreads();
-  const int r = incl + sh[warp];
+  const uint32_t r = incl + sh[warp];
   __syncthreads();
   return r;
 }
@@ -94,7 +98,7 @@ __device__ __forceinline__ void radix_pass(const uint32_t* keys, int cnt, int sh
   const int b0 = nb - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
   const int h0 = b0 >= 0 ? sh.hist[b0] : 0;
   const int h1 = b1 >= 0 ? sh.hist[b1] : 0;
-  const int incl = block_incl_scan(h0 + h1, sh.scan);
+  const int incl = (int)block_incl_scan((uint32_t)(h0 + h1), sh.scan);
   const int before = incl - h0 - h1;
   if (before < remaining && incl >= remaining) {
     if (before + h0 >= remaining) {
@@ -153,96 +157,66 @@ __device__ __forceinline__ void select_threshold(const uint32_t* keys, int cnt, 
 }
 
 // Emit the kept positions in ascending order: every key > T and the first
-// `need` keys == T (position order).  pos_of(i) maps a key index to its
-// position.  Each warp takes a contiguous segment (a multiple of 128 keys);
-// per step a lane holds four consecutive keys and one warp scan of packed
-// (greater, equal) counts places them.
+// `need` keys == T (position order); all keys when take_all.  pos_of(i) maps
+// a key index to its position.  One pass over the keys builds two bit masks
+// per 32 consecutive keys (a warp ballot each: > T, == T); one block scan of
+// the packed per-word counts (greater | equal << 16) then gives every word its
+// output offset and its rank among the equal keys, and each thread writes the
+// kept positions of its two words.  Every key is read once.
 template <typename PosOf>
 __device__ __forceinline__ void emit(const uint32_t* keys, int cnt, uint32_t T, int need,
                                      bool take_all, int32_t* out_pos, uint32_t* out_key,
                                      PosOf pos_of, Shared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int seg = ((cnt + kThreads * 4 - 1) / (kThreads * 4)) * 128;
-  const int s0 = warp * seg, s1 = min(cnt, s0 + seg);
-  int gt = 0, eq = 0;
-  for (int base = s0; base < s1; base += 128) {
-    const int i0 = base + 4 * lane;
-    const uint4 v = i0 < s1 ? k4[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i0 + e < s1) {
-        gt += take_all || kv[e] > T;
-        eq += !take_all && kv[e] == T;
-      }
+  const int nwords = (cnt + 31) >> 5;
+  for (int wd = warp; wd < nwords; wd += kWarps) {
+    const int i = wd * 32 + lane;
+    const uint32_t k = i < cnt ? keys[i] : 0u;
+    const bool in = i < cnt;
+    const uint32_t g = __ballot_sync(0xffffffffu, in && (take_all || k > T));
+    const uint32_t e = __ballot_sync(0xffffffffu, in && !take_all && k == T);
+    if (lane == 0) {
+      sh.gtm[wd] = g;
+      sh.eqm[wd] = e;
     }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  if (lane == 0) {
-    sh.wgt[warp] = gt;
-    sh.weq[warp] = eq;
   }
   __syncthreads();
-  if (warp == 0) {
-    const int g = sh.wgt[lane], e = sh.weq[lane];
-    int gi = g, ei = e;
+  // thread t owns words 2t and 2t + 1
+  const int w0 = 2 * (int)threadIdx.x, w1 = w0 + 1;
+  const uint32_t g0 = w0 < nwords ? sh.gtm[w0] : 0u, e0 = w0 < nwords ? sh.eqm[w0] : 0u;
+  const uint32_t g1 = w1 < nwords ? sh.gtm[w1] : 0u, e1 = w1 < nwords ? sh.eqm[w1] : 0u;
+  // packed (greater | equal << 16): each field stays below kCap < 2^16, so the
+  // sums never carry between fields; unsigned, since equal << 16 may pass 2^31
+  const uint32_t c0 = (uint32_t)__popc(g0) | ((uint32_t)__popc(e0) << 16);
+  const uint32_t c1 = (uint32_t)__popc(g1) | ((uint32_t)__popc(e1) << 16);
+  const uint32_t incl = block_incl_scan(c0 + c1, sh.scan);
+  uint32_t before = incl - c0 - c1;  // packed counts of the earlier words
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t1 = __shfl_up_sync(0xffffffffu, gi, o);
-      const int t2 = __shfl_up_sync(0xffffffffu, ei, o);
-      if (lane >= o) {
-        gi += t1;
-        ei += t2;
-      }
+  for (int h = 0; h < 2; ++h) {
+    const int wd = h ? w1 : w0;
+    if (wd >= nwords) break;
+    const uint32_t g = h ? g1 : g0;
+    uint32_t e = h ? e1 : e0;
+    const int gt_before = (int)(before & 0xFFFFu), eq_before = (int)(before >> 16);
+    // keep the first (need - eq_before) keys == T of this word
+    int keep_eq = need - eq_before;
+    uint32_t ek = 0u;
+    for (; keep_eq > 0 && e; --keep_eq) {
+      const uint32_t lowest = e & (0u - e);
+      ek |= lowest;
+      e ^= lowest;
     }
-    sh.wgt[lane] = gi - g;  // exclusive
-    sh.weq[lane] = ei - e;
-  }
-  __syncthreads();
-  int eq_seen = sh.weq[warp];  // keys == T before this step, in position order
-  int w = sh.wgt[warp] + max(0, min(eq_seen, need));
-  for (int base = s0; base < s1; base += 128) {
-    const int i0 = base + 4 * lane;
-    const uint4 v = i0 < s1 ? k4[i0 >> 2] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-    int cg = 0, cq = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i0 + e < s1) {
-        cg += take_all || kv[e] > T;
-        cq += !take_all && kv[e] == T;
-      }
+    uint32_t m = g | ek;
+    int o = gt_before + min(max(need, 0), eq_before);
+    while (m) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1;
+      const int i = wd * 32 + b;
+      out_pos[o] = pos_of(i);
+      if (out_key) out_key[o] = keys[i];
+      ++o;
     }
-    const int packed = cg | (cq << 16);
-    int incl = packed;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int excl = incl - packed;
-    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-    int eqr = eq_seen + (excl >> 16);  // rank among keys == T of this lane's first one
-    int o = w + (excl & 0xFFFF) + max(0, min(excl >> 16, need - eq_seen));
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i0 + e < s1) {
-        bool keep = take_all || kv[e] > T;
-        if (!take_all && kv[e] == T) keep = eqr++ < need;
-        if (keep) {
-          out_pos[o] = pos_of(i0 + e);
-          if (out_key) out_key[o] = kv[e];
-          ++o;
-        }
-      }
-    }
-    w += (tot & 0xFFFF) + max(0, min(tot >> 16, need - eq_seen));
-    eq_seen += tot >> 16;
+    before += h ? 0 : c0;
   }
 }
 
