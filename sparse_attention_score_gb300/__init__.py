@@ -349,7 +349,10 @@ class Pipeline:
         self.layout, self.kind, self.K = layout, kind, int(K)
         self.prefill_seq = prefill_seq
         self.Nq, self.Hq, self.Dqk, self.Dv = int(Nq), int(Hq), int(Dqk), int(Dv)
-        self.ld = int(ld if ld is not None else max(layout.max_seq_len, 1))
+        # default row stride: the longest row rounded up to 4 scores, so that
+        # every row starts on a 16-byte boundary (top-K then loads it with
+        # 16-byte copies)
+        self.ld = int(ld if ld is not None else (max(layout.max_seq_len, 1) + 3) // 4 * 4)
         self.scores = torch.empty((self.Nq, self.ld), dtype=torch.float32, device=device)
         self.idx = torch.empty((self.Nq, self.K), dtype=torch.int32, device=device)
         self.out = torch.empty((self.Nq, Hq, Dv), dtype=torch.bfloat16, device=device)

@@ -42,6 +42,14 @@ struct Shared {
   int chunk_off[33];
 };
 
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+
 // Inclusive block scan of one unsigned value per thread (sums wrap modulo
 // 2^32, which packed counts rely on); returns the inclusive value.
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* sh) {
@@ -248,12 +256,42 @@ __global__ void __launch_bounds__(kThreads, 2)
     const long long rem = n - start;
     cnt = (int)(rem < 0 ? 0 : (rem > kCap ? kCap : rem));
     const float* src = a.scores + (long long)r * a.ld + start;
+    if ((((uintptr_t)src) & 15u) == 0) {
+      // the whole block in flight at once (16-byte copies), then the scores
+      // are turned into keys in place
+      const int n4 = cnt >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+      for (int j = threadIdx.x; j < n4; j += kThreads) cp_async16(keys + 4 * j, s4 + j);
+      for (int i = 4 * n4 + threadIdx.x; i < cnt; i += kThreads)
+        keys[i] = __float_as_uint(__ldg(&src[i]));
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncthreads();
+      uint4* k4 = reinterpret_cast<uint4*>(keys);
+#pragma unroll 4
+      for (int j = threadIdx.x; j < n4; j += kThreads) {
+        uint4 v = k4[j];
+        v.x = score_key(__uint_as_float(v.x));
+        v.y = score_key(__uint_as_float(v.y));
+        v.z = score_key(__uint_as_float(v.z));
+        v.w = score_key(__uint_as_float(v.w));
+        k4[j] = v;
+        kmin = min(min(kmin, min(v.x, v.y)), min(v.z, v.w));
+        kmax = max(max(kmax, max(v.x, v.y)), max(v.z, v.w));
+      }
+      for (int i = 4 * n4 + threadIdx.x; i < cnt; i += kThreads) {
+        const uint32_t k = score_key(__uint_as_float(keys[i]));
+        keys[i] = k;
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
+    } else {
 #pragma unroll 8
-    for (int i = threadIdx.x; i < cnt; i += kThreads) {
-      const uint32_t k = score_key(__ldg(&src[i]));
-      keys[i] = k;
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
+      for (int i = threadIdx.x; i < cnt; i += kThreads) {
+        const uint32_t k = score_key(__ldg(&src[i]));
+        keys[i] = k;
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
     }
   } else {
     if (threadIdx.x == 0) {
