@@ -775,6 +775,11 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   long long grid = sm_count();
   if (grid > kMaxCtas) grid = kMaxCtas;
   if (grid > g.total) grid = g.total;
+  // As few CTAs as give every CTA the same largest share: with 512 tiles on
+  // 152 SMs some CTA takes 4 tiles either way, and 128 CTAs of exactly 4 keep
+  // each CTA inside one query (one finalize, fewer partials to merge).
+  const long long per = (g.total + grid - 1) / grid;
+  grid = (g.total + per - 1) / per;
   g.G = (int)grid;
   g.lo = g.hi = 0;
   cudaError_t e =
