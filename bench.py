@@ -224,6 +224,20 @@ def algorithmic(case):
                 attn_flops=attn_flops)
 
 
+# ------------------------------------------------------------- multi-rank --
+def max_over_ranks(value, world, device):
+    """The slowest rank's value (weak scaling: every rank times its own batch,
+    the job takes as long as the slowest); a barrier follows, so no rank
+    leaves before all have reported."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- GPU arm --
 def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     import torch
@@ -326,11 +340,7 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     if do_e2e:
         e2e = run_e2e(case, d, pipe, graphs["step"], steps, dev, flush)
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        torch.distributed.barrier()
+    total_ms = max_over_ranks(total_ms, world, dev)
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
                 launches=int(launches), launches_per=launches_per, clocks=clocks, status=status,
                 e2e=e2e, graph=graphs["step"], cache_write=cache_write)
