@@ -290,21 +290,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ql = g * kGroupQ + 2 * half + j;  // query within the block
             const uint32_t taddr = tbase + ((uint32_t)(quad * 32) << 16) + acc * 256 +
                                    half * 128 + j * kHeads;
-            uint32_t v[32];
+            // both 32-column halves in flight before one wait
+            uint32_t v[32], v2[32];
             float s0 = 0.0f, s1 = 0.0f;
             tmem_ld_32cols(taddr, v);
+            tmem_ld_32cols(taddr + 32, v2);
             tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 32; h += 2) {
               s0 = fmaf(s.w[ql][h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
               s1 = fmaf(s.w[ql][h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
             }
-            tmem_ld_32cols(taddr + 32, v);
-            tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 32; h += 2) {
-              s0 = fmaf(s.w[ql][32 + h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
-              s1 = fmaf(s.w[ql][33 + h], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+              s0 = fmaf(s.w[ql][32 + h], fmaxf(__uint_as_float(v2[h]), 0.0f), s0);
+              s1 = fmaf(s.w[ql][33 + h], fmaxf(__uint_as_float(v2[h + 1]), 0.0f), s1);
             }
             sc[j] = (s0 + s1) + 0.0f;
           }
