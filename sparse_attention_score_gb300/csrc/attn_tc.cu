@@ -663,10 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // grid is idle.  Each thread owns two float4 of dv for one of the group's 4
 // heads and reads, for up to kMergeBatch slots at a time, the slot's (m, l)
 // and its two partial float4 in one go: a query split over at most
-// kMergeBatch CTAs is merged after a single round trip.  Slots beyond the
-// first batch are folded in with a running maximum.
+// kMergeBatch CTAs (a decode query over four CTAs of four tiles) is merged
+// after a single round trip.  Slots beyond the first batch are folded in with
+// a running maximum.  Four slots per batch keep the kernel at 80 registers,
+// three blocks per SM.
 constexpr int kMergeHeads = 4;
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 4;
 
 __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, const float* part_o,
                                                        const float* part_ml, int by_query) {
