@@ -329,11 +329,19 @@ int dsa_prefill_step(const dsa_paged_layout* layout, int seq, const int32_t* q_p
  * dsa_last_error_string: message of the last failing call on this host thread.
  * dsa_launch_count: kernels this library has launched in this process.
  * dsa_version: 10000*major + 100*minor + patch.
+ * dsa_selftest_bounded_wait: one bounded mbarrier wait of the kind every
+ *   pipelined kernel uses (one thread of one CTA).  expire != 0: nothing
+ *   arrives, the wait gives up after limit_ns (1 us .. 1 s) and
+ *   DSA_STATUS_TIMEOUT is OR-ed into the status word of ws (>= 256 bytes);
+ *   expire == 0: the barrier completes first and nothing is recorded.  For
+ *   testing the give-up path without a hang; the context stays usable.
  */
 int dsa_get_status(void* ws, dsa_stream_t stream, int32_t* status, int clear);
 const char* dsa_last_error_string(void);
 uint64_t dsa_launch_count(void);
 int dsa_version(void);
+int dsa_selftest_bounded_wait(int expire, uint64_t limit_ns, void* ws, size_t ws_bytes,
+                              dsa_stream_t stream);
 
 #ifdef __cplusplus
 }

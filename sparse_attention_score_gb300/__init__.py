@@ -77,6 +77,7 @@ _sig("dsa_version", _i, [])
 _sig("dsa_launch_count", ctypes.c_uint64, [])
 _sig("dsa_last_error_string", ctypes.c_char_p, [])
 _sig("dsa_get_status", _i, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), _i])
+_sig("dsa_selftest_bounded_wait", _i, [_i, ctypes.c_uint64, _vp, _sz, _vp])
 _sig("dsa_index_score_workspace_size", _sz, [_i, _i, _i, _i64])
 _sig("dsa_index_score", _i, [_LP, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _i64, _vp, _sz, _vp])
 _sig("dsa_index_score_prefill_workspace_size", _sz, [_i, _i, _i, _i64])
@@ -102,6 +103,7 @@ _sig("dsa_sparse_attn_prefill", _i, [_LP, _vp, _vp, _i64, _vp, _i64, _i, _i, _i,
                                      _i, _f, _vp, _vp, _vp, _sz, _vp])
 
 SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_status",
+           "dsa_selftest_bounded_wait",
            "dsa_index_score_workspace_size", "dsa_index_score",
            "dsa_index_score_prefill_workspace_size", "dsa_index_score_prefill",
            "dsa_topk_workspace_size",

@@ -267,6 +267,16 @@ int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const
                      q_pos, Nq, idx, K, sm_scale, out, lse, ws, ws_bytes, stream, false);
 }
 
+int dsa_selftest_bounded_wait(int expire, uint64_t limit_ns, void* ws, size_t ws_bytes,
+                              dsa_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull)
+    return set_error(DSA_ERR_INVALID, "selftest_bounded_wait: limit_ns must be in [1 us, 1 s]");
+  int rc = check_ws(ws, ws_bytes, kWsHeader);
+  if (rc) return rc;
+  return bounded_wait_selftest(expire ? 1 : 0, (unsigned long long)limit_ns,
+                               reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------- steps --
 // A step workspace: the step's status header, then one region per stage
 // (each region 256-byte aligned and laid out as that stage's own workspace).

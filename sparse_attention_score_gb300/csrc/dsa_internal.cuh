@@ -89,6 +89,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// selftest.cu
+int bounded_wait_selftest(int expire, unsigned long long limit_ns, int* status, cudaStream_t s);
+
 // cache_write.cu
 int cache_write(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, int N,
                 const void* kv_new, int row_elems, void* kv_pool, long long kv_row_stride,
