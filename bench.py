@@ -338,7 +338,7 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
 
     e2e = None
     if do_e2e:
-        e2e = run_e2e(case, d, pipe, graphs["step"], steps, dev, flush)
+        e2e = run_e2e(case, d, pipe, steps, dev, flush)
 
     total_ms = max_over_ranks(total_ms, world, dev)
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
@@ -390,7 +390,7 @@ def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
             "status": dsa.get_status(ws)}
 
 
-def run_e2e(case, d, pipe, graph, steps, dev, flush):
+def run_e2e(case, d, pipe, steps, dev, flush):
     """The same step end to end through the C ABI calls with host buffers:
     H2D of the step's inputs (queries, indexer queries, weights, block table,
     lengths) from pinned memory, the three stages, D2H of the attention

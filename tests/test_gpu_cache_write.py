@@ -23,14 +23,8 @@ LAT_SHAPES = dict(Hq=64, Dqk=576, Dv=512, latent=True, H_i=64, D_i=128, idx_dtyp
 TINY_SHAPES = dict(Hq=16, Dqk=128, Dv=128, latent=False, H_i=4, D_i=64, idx_dtype="bf16")
 
 
-_logical = logical_rows
-_dev = to_dev
-_host = to_host
-_fresh_layout = fresh_layout
-
-
 def _write(dsa, layout, seq, pos, kv_rows, kv_pool, ki_rows, ki_pool, ws):
-    dsa.cache_write(layout, _dev(seq), _dev(pos), ws, kv_new=kv_rows, kv_pool=kv_pool,
+    dsa.cache_write(layout, to_dev(seq), to_dev(pos), ws, kv_new=kv_rows, kv_pool=kv_pool,
                     kidx_new=ki_rows, kidx_pool=ki_pool)
 
 
@@ -43,14 +37,14 @@ def test_cache_write_bulk_prefill_is_byte_exact(shapes, lens, stride_pad):
     need_gpu()
     dsa = lib()
     c = W.make_case("cw", seed=500 + len(lens), seq_lens=lens, K=64, **shapes)
-    bt2, nb2 = _fresh_layout(c, 17 + len(lens), 3)
+    bt2, nb2 = fresh_layout(c, 17 + len(lens), 3)
     rng = np.random.default_rng(23)
     seq = np.concatenate([np.full(int(L), b, np.int32) for b, L in enumerate(c.seq_lens)])
     pos = np.concatenate([np.arange(int(L), dtype=np.int32) for L in c.seq_lens])
     order = rng.permutation(seq.shape[0])
     seq, pos = seq[order], pos[order]
-    kv_rows = np.concatenate([_logical(c, c.k_pool, b, int(L)) for b, L in enumerate(c.seq_lens)])
-    ki_rows = np.concatenate([_logical(c, c.kidx_pool, b, int(L))
+    kv_rows = np.concatenate([logical_rows(c, c.k_pool, b, int(L)) for b, L in enumerate(c.seq_lens)])
+    ki_rows = np.concatenate([logical_rows(c, c.kidx_pool, b, int(L))
                               for b, L in enumerate(c.seq_lens)])
     kv_rows, ki_rows = kv_rows[order], ki_rows[order]
     W_ = c.Dkv + stride_pad
@@ -60,15 +54,15 @@ def test_cache_write_bulk_prefill_is_byte_exact(shapes, lens, stride_pad):
     ki_want, bad2 = oracle.cache_write(bt2, c.bs, nb2, seq, pos, ki_rows, ki0)
     assert not bad1 and not bad2
 
-    lay = dsa.PagedLayout(_dev(bt2), _dev(c.seq_lens), c.bs, nb2, c.max_len)
-    kv_pool, ki_pool = _dev(kv0), _dev(ki0)
+    lay = dsa.PagedLayout(to_dev(bt2), to_dev(c.seq_lens), c.bs, nb2, c.max_len)
+    kv_pool, ki_pool = to_dev(kv0), to_dev(ki0)
     ws = dsa.workspace(dsa.cache_write_workspace_size())
     n0 = dsa.launch_count()
-    _write(dsa, lay, seq, pos, _dev(kv_rows), kv_pool, _dev(ki_rows), ki_pool, ws)
+    _write(dsa, lay, seq, pos, to_dev(kv_rows), kv_pool, to_dev(ki_rows), ki_pool, ws)
     assert dsa.launch_count() == n0 + 1
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(_host(kv_pool, kv0), kv_want)
-    np.testing.assert_array_equal(_host(ki_pool, ki0), ki_want)
+    np.testing.assert_array_equal(to_host(kv_pool, kv0), kv_want)
+    np.testing.assert_array_equal(to_host(ki_pool, ki0), ki_want)
     assert dsa.get_status(ws) == 0
 
 
@@ -92,11 +86,12 @@ def test_cache_write_decode_append_then_pipeline_matches_oracle():
     ws = dsa.workspace(dsa.cache_write_workspace_size())
     _write(dsa, g.layout, seq, last, garbage_kv, g.d.k_pool, garbage_ki, g.d.kidx_pool, ws)
     torch.cuda.synchronize()
-    assert not np.array_equal(_host(g.d.k_pool, c.k_pool), c.k_pool)
-    _write(dsa, g.layout, seq, last, _dev(kv_rows), g.d.k_pool, _dev(ki_rows), g.d.kidx_pool, ws)
+    assert not np.array_equal(to_host(g.d.k_pool, c.k_pool), c.k_pool)
+    _write(dsa, g.layout, seq, last, to_dev(kv_rows), g.d.k_pool, to_dev(ki_rows),
+           g.d.kidx_pool, ws)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(_host(g.d.k_pool, c.k_pool), c.k_pool)
-    np.testing.assert_array_equal(_host(g.d.kidx_pool, c.kidx_pool), c.kidx_pool)
+    np.testing.assert_array_equal(to_host(g.d.k_pool, c.k_pool), c.k_pool)
+    np.testing.assert_array_equal(to_host(g.d.kidx_pool, c.kidx_pool), c.kidx_pool)
     s = g.scores().cpu().numpy()
     s_ref = oracle_scores(c, ld=s.shape[1])
     assert_scores_equal(s, s_ref, c.n_elig)
@@ -117,15 +112,15 @@ def test_cache_write_prefill_written_cache_serves_decode():
     dsa = lib()
     T = 3000
     c = W.make_case("cw-prefill", seed=520, seq_lens=(T,), K=2048, **LAT_SHAPES)
-    bt2, nb2 = _fresh_layout(c, 29, 2)
+    bt2, nb2 = fresh_layout(c, 29, 2)
     seq = np.zeros(T, np.int32)
     pos = np.arange(T, dtype=np.int32)
-    lay = dsa.PagedLayout(_dev(bt2), _dev(c.seq_lens), c.bs, nb2, c.max_len)
+    lay = dsa.PagedLayout(to_dev(bt2), to_dev(c.seq_lens), c.bs, nb2, c.max_len)
     kv_pool = torch.zeros((nb2, c.bs, c.Dkv), dtype=torch.bfloat16, device="cuda")
     ki_pool = torch.zeros((nb2, c.bs, c.D_i), dtype=torch.uint8, device="cuda")
     ws = dsa.workspace(dsa.cache_write_workspace_size())
-    _write(dsa, lay, seq, pos, _dev(_logical(c, c.k_pool, 0, T)), kv_pool,
-           _dev(_logical(c, c.kidx_pool, 0, T)), ki_pool, ws)
+    _write(dsa, lay, seq, pos, to_dev(logical_rows(c, c.k_pool, 0, T)), kv_pool,
+           to_dev(logical_rows(c, c.kidx_pool, 0, T)), ki_pool, ws)
     d = wdev.upload(c)
     pipe = dsa.Pipeline(lay, kind="decode", Nq=c.Nq, Hq=c.Hq, Dqk=c.Dqk, Dv=c.Dv, H_i=c.H_i,
                         D_i=c.D_i, K=c.K)
@@ -160,13 +155,13 @@ def test_cache_write_flags_rows_without_a_destination():
     kv_want, bad = oracle.cache_write(bt, c.bs, c.num_blocks, seq, pos, kv_rows, c.k_pool)
     ki_want, _ = oracle.cache_write(bt, c.bs, c.num_blocks, seq, pos, ki_rows, c.kidx_pool)
     assert bad
-    lay = dsa.PagedLayout(_dev(bt), _dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
-    kv_pool, ki_pool = _dev(c.k_pool), _dev(c.kidx_pool)
+    lay = dsa.PagedLayout(to_dev(bt), to_dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
+    kv_pool, ki_pool = to_dev(c.k_pool), to_dev(c.kidx_pool)
     ws = dsa.workspace(dsa.cache_write_workspace_size())
-    _write(dsa, lay, seq, pos, _dev(kv_rows), kv_pool, _dev(ki_rows), ki_pool, ws)
+    _write(dsa, lay, seq, pos, to_dev(kv_rows), kv_pool, to_dev(ki_rows), ki_pool, ws)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(_host(kv_pool, c.k_pool), kv_want)
-    np.testing.assert_array_equal(_host(ki_pool, c.kidx_pool), ki_want)
+    np.testing.assert_array_equal(to_host(kv_pool, c.k_pool), kv_want)
+    np.testing.assert_array_equal(to_host(ki_pool, c.kidx_pool), ki_want)
     assert dsa.get_status(ws) == 1                                # DSA_STATUS_BAD_BLOCK
     assert dsa.get_status(ws) == 0                                # cleared by the read
 
@@ -178,11 +173,11 @@ def test_cache_write_duplicates_leave_one_of_the_rows():
     seq = np.zeros(64, np.int32)
     pos = np.full(64, 17, np.int32)
     rows = np.repeat(np.arange(64, dtype=np.uint16)[:, None] + 1, c.Dkv, axis=1)
-    lay = dsa.PagedLayout(_dev(c.block_table), _dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
-    kv_pool = _dev(c.k_pool)
+    lay = dsa.PagedLayout(to_dev(c.block_table), to_dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
+    kv_pool = to_dev(c.k_pool)
     ws = dsa.workspace(dsa.cache_write_workspace_size())
-    dsa.cache_write(lay, _dev(seq), _dev(pos), ws, kv_new=_dev(rows), kv_pool=kv_pool)
-    got = _host(kv_pool, c.k_pool)
+    dsa.cache_write(lay, to_dev(seq), to_dev(pos), ws, kv_new=to_dev(rows), kv_pool=kv_pool)
+    got = to_host(kv_pool, c.k_pool)
     page = c.block_table[0, 0]
     row = got[page, 17]
     assert any(np.array_equal(row, rows[i]) for i in range(64))
@@ -195,11 +190,11 @@ def test_cache_write_host_errors_launch_nothing():
     need_gpu()
     dsa = lib()
     c = W.make_case("cw-err", seed=550, seq_lens=(64,), bs=64, K=8, **TINY_SHAPES)
-    lay = dsa.PagedLayout(_dev(c.block_table), _dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
-    kv_pool = _dev(c.k_pool)
+    lay = dsa.PagedLayout(to_dev(c.block_table), to_dev(c.seq_lens), c.bs, c.num_blocks, c.max_len)
+    kv_pool = to_dev(c.k_pool)
     ws = dsa.workspace(dsa.cache_write_workspace_size())
-    seq = _dev(np.zeros(4, np.int32))
-    pos = _dev(np.arange(4, dtype=np.int32))
+    seq = to_dev(np.zeros(4, np.int32))
+    pos = to_dev(np.arange(4, dtype=np.int32))
     L = dsa.lib()
     n0 = dsa.launch_count()
     vp = ctypes.c_void_p
