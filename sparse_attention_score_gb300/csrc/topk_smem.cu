@@ -83,25 +83,53 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* sh) {
 // key.  Updates prefix/mask/remaining.  Keys are read four at a time; the
 // digits below the bits shared by every key of the block are diverse enough
 // that plain shared atomics rarely collide.
+// Also returns, over the keys matching (prefix, mask) on entry, the OR and the
+// AND of their bits: where the two agree below the digit, every candidate
+// shares those bits, and so does the threshold.
 __device__ __forceinline__ void radix_pass(const uint32_t* keys, int cnt, int shift, int bits,
                                            uint32_t& prefix, uint32_t& mask, int& remaining,
-                                           Shared& sh) {
+                                           uint32_t& cand_or, uint32_t& cand_and, Shared& sh) {
   const int nb = 1 << bits;
   for (int i = threadIdx.x; i < nb; i += kThreads) sh.hist[i] = 0;
   __syncthreads();
   const uint4* k4 = reinterpret_cast<const uint4*>(keys);
   const int n4 = (cnt + 3) >> 2;  // the array has room for three keys past cnt
   const uint32_t dm = (uint32_t)(nb - 1);
+  uint32_t c_or = 0u, c_and = 0xFFFFFFFFu;
 #pragma unroll 4
   for (int j = threadIdx.x; j < n4; j += kThreads) {
     const uint4 v = k4[j];
     const int i0 = 4 * j;
-    if ((v.x & mask) == prefix) atomicAdd(&sh.hist[(v.x >> shift) & dm], 1);
-    if (i0 + 1 < cnt && (v.y & mask) == prefix) atomicAdd(&sh.hist[(v.y >> shift) & dm], 1);
-    if (i0 + 2 < cnt && (v.z & mask) == prefix) atomicAdd(&sh.hist[(v.z >> shift) & dm], 1);
-    if (i0 + 3 < cnt && (v.w & mask) == prefix) atomicAdd(&sh.hist[(v.w >> shift) & dm], 1);
+    if ((v.x & mask) == prefix) {
+      atomicAdd(&sh.hist[(v.x >> shift) & dm], 1);
+      c_or |= v.x;
+      c_and &= v.x;
+    }
+    if (i0 + 1 < cnt && (v.y & mask) == prefix) {
+      atomicAdd(&sh.hist[(v.y >> shift) & dm], 1);
+      c_or |= v.y;
+      c_and &= v.y;
+    }
+    if (i0 + 2 < cnt && (v.z & mask) == prefix) {
+      atomicAdd(&sh.hist[(v.z >> shift) & dm], 1);
+      c_or |= v.z;
+      c_and &= v.z;
+    }
+    if (i0 + 3 < cnt && (v.w & mask) == prefix) {
+      atomicAdd(&sh.hist[(v.w >> shift) & dm], 1);
+      c_or |= v.w;
+      c_and &= v.w;
+    }
+  }
+  c_or = __reduce_or_sync(0xffffffffu, c_or);
+  c_and = __reduce_and_sync(0xffffffffu, c_and);
+  if ((threadIdx.x & 31) == 0) {
+    sh.wgt[threadIdx.x >> 5] = (int)c_or;
+    sh.weq[threadIdx.x >> 5] = (int)c_and;
   }
   __syncthreads();
+  cand_or = __reduce_or_sync(0xffffffffu, (uint32_t)sh.wgt[threadIdx.x & 31]);
+  cand_and = __reduce_and_sync(0xffffffffu, (uint32_t)sh.weq[threadIdx.x & 31]);
   // thread t owns bins nb-1-2t and nb-2-2t (highest digits first)
   const int b0 = nb - 1 - 2 * (int)threadIdx.x, b1 = b0 - 1;
   const int h0 = b0 >= 0 ? sh.hist[b0] : 0;
@@ -159,7 +187,16 @@ __device__ __forceinline__ void select_threshold(const uint32_t* keys, int cnt, 
   while (hi >= 0) {
     const int bits = hi + 1 < 11 ? hi + 1 : 11;
     const int shift = hi + 1 - bits;
-    radix_pass(keys, cnt, shift, bits, prefix, mask, remaining, sh);
+    uint32_t cand_or, cand_and;
+    radix_pass(keys, cnt, shift, bits, prefix, mask, remaining, cand_or, cand_and, sh);
+    // the bits below this digit, where every candidate agrees, need no pass
+    // (integer-valued scores leave their low mantissa bits zero)
+    const uint32_t below = shift > 0 ? (1u << shift) - 1u : 0u;
+    if (below && ((cand_or ^ cand_and) & below) == 0u) {
+      prefix |= cand_and & below;
+      mask |= below;
+      break;
+    }
     hi = shift - 1;
   }
 }
