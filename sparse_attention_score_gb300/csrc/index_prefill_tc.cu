@@ -12,11 +12,12 @@
 // 128 KB) stay in shared memory while the block's key tiles stream past:
 // per 128-position tile, four tcgen05.mma.kind::f8f6f4 groups of N = 256
 // (4 queries x 64 heads) accumulate into two alternating 256-column TMEM
-// buffers.  Eight epilogue warps (two per TMEM lane quadrant, one per half of
-// the columns) apply ReLU, the head weights and the head sum, and store the
-// scores of the causal positions.  Work items (block, key tile) are laid end
+// buffers.  Sixteen epilogue warps (four per TMEM lane quadrant, one per
+// query of the group's four) apply ReLU, the head weights and the head sum,
+// and store the scores of the causal positions; the epilogue is bound by its
+// instruction latency, so more warps per quadrant hide more of it.  Work items (block, key tile) are laid end
 // to end and split evenly over one CTA per SM, which balances the triangle.
-// Warp roles: 0-7 epilogue, 8 TMA producer, 9 TMEM owner + MMA issuer.
+// Warp roles: 0-15 epilogue, 16 TMA producer, 17 TMEM owner + MMA issuer.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
@@ -39,7 +40,11 @@ constexpr int kTileBytes = kTileRows * kRowBytes;
 constexpr int kPageBytes = 64 * kRowBytes;
 constexpr int kGroupBytes = kGroupQ * kHeads * kRowBytes;  // 32 KB
 constexpr int kMaxBlocks = 2048;                           // Nq <= 32768
-constexpr int kThreads = 320;
+constexpr int kEpiWarps = 16;                              // epilogue warps
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kQPerWarp = kGroupQ / (kEpiWarps / 4);       // queries per epilogue warp
+constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kThreads = kEpiThreads + 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc(128, kGroupQ * kHeads, 0, 0);
 
@@ -93,17 +98,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.bempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.accfull[i], 1);
-      mbar_init(&s.accempty[i], 256);
+      mbar_init(&s.accempty[i], kEpiThreads);
     }
     mbar_init(&s.done, 1);
-    mbar_init(&s.epsync, 256);
+    mbar_init(&s.epsync, kEpiThreads);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_q);
   }
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return l;
   };
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && lo < hi) {
       int bi = block_of(lo), cur = -1, nbl = 0, stage = 0, issued = 0;
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&s.full[st], issued_parity[st], &s.abort, 100000000ull);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && lo < hi) {
       int bi = block_of(lo), cur = -1, nbl = 0, stage = 0, it = 0;
@@ -246,13 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue --
-    const int quad = warp & 3, half = warp >> 2;  // lanes 32*quad.., columns 128*half..
-    const int et = threadIdx.x;                    // 0..255
+    const int quad = warp & 3, qsel = warp >> 2;  // lanes 32*quad.., queries kQPerWarp*qsel..
+    const int et = threadIdx.x;                    // 0..kEpiThreads-1
     uint32_t ep = 0;
     if (lo < hi) {
       int bi = block_of(lo), cur = -1, it = 0;
       bool ok = true;
-      long long n_q[2 * kGroups];  // eligible counts of this thread's 8 queries
+      long long n_q[kQPerWarp * kGroups];  // eligible counts of this thread's queries
       for (int item = lo; item < hi && ok; ++item) {
         while (s.prefix[bi + 1] <= item) ++bi;
         if (bi != cur) {
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&s.epsync);
           if (!warp_wait(&s.epsync, ep, &s.abort)) { ok = false; break; }
           ep ^= 1;
-          for (int i = et; i < kQB * kHeads; i += 256) {
+          for (int i = et; i < kQB * kHeads; i += kEpiThreads) {
             const int r = bi * kQB + i / kHeads;
             s.w[i / kHeads][i % kHeads] = r < a.Nq ? __ldg(&a.w[(long long)r * kHeads + i % kHeads]) : 0.0f;
           }
@@ -270,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int g = 0; g < kGroups; ++g)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              n_q[2 * g + j] = elig(a, L, bi * kQB + g * kGroupQ + 2 * half + j);
+            for (int j = 0; j < kQPerWarp; ++j)
+              n_q[kQPerWarp * g + j] = elig(a, L, bi * kQB + g * kGroupQ + kQPerWarp * qsel + j);
           cur = bi;
         }
         const long long p = (long long)(item - s.prefix[bi]) * kTileRows + quad * 32 + lane;
@@ -284,36 +289,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int acc = it & 1;
           if (!warp_wait(&s.accfull[acc], (it >> 1) & 1, &s.abort)) { ok = false; break; }
           tc_fence_after();
-          float sc[2] = {0.0f, 0.0f};
+          float sc[kQPerWarp];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int ql = g * kGroupQ + 2 * half + j;  // query within the block
+          for (int j = 0; j < kQPerWarp; ++j) {
+            const int ql = g * kGroupQ + kQPerWarp * qsel + j;  // query within the block
             const uint32_t taddr = tbase + ((uint32_t)(quad * 32) << 16) + acc * 256 +
-                                   half * 128 + j * kHeads;
-            // both 32-column halves in flight before one wait
-            uint32_t v[32], v2[32];
+                                   (kQPerWarp * qsel + j) * kHeads;
+            uint32_t v[32];
             float s0 = 0.0f, s1 = 0.0f;
-            tmem_ld_32cols(taddr, v);
-            tmem_ld_32cols(taddr + 32, v2);
-            tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; h += 2) {
-              s0 = fmaf(s.w[ql][h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
-              s1 = fmaf(s.w[ql][h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
-            }
+            for (int hh = 0; hh < 2; ++hh) {
+              tmem_ld_32cols(taddr + 32 * hh, v);
+              tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; h += 2) {
-              s0 = fmaf(s.w[ql][32 + h], fmaxf(__uint_as_float(v2[h]), 0.0f), s0);
-              s1 = fmaf(s.w[ql][33 + h], fmaxf(__uint_as_float(v2[h + 1]), 0.0f), s1);
+              for (int h = 0; h < 32; h += 2) {
+                s0 = fmaf(s.w[ql][32 * hh + h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
+                s1 = fmaf(s.w[ql][32 * hh + h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+              }
             }
             sc[j] = (s0 + s1) + 0.0f;
           }
           tc_fence_before();
           mbar_arrive(&s.accempty[acc]);
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int r = bi * kQB + g * kGroupQ + 2 * half + j;
-            if (p < n_q[2 * g + j]) {
+          for (int j = 0; j < kQPerWarp; ++j) {
+            const int r = bi * kQB + g * kGroupQ + kQPerWarp * qsel + j;
+            if (p < n_q[kQPerWarp * g + j]) {
               float out = sc[j];
               if (!page_ok) {
                 flag_status(a.status, DSA_STATUS_BAD_BLOCK);
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
