@@ -30,8 +30,10 @@
 // partial (O, m, l) per CTA in the workspace and a second small kernel merges
 // them:  M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
 //
-// Warp roles (320 threads):
-//   warps 0-3 softmax, and at the end of each query segment O out of TMEM;
+// Warp roles (448 threads):
+//   warps 0-3 and 10-13 softmax, and at the end of each query segment O out
+//   of TMEM: two warps per TMEM lane quadrant, one for heads 0-31 and one for
+//   heads 32-63, which halves the softmax's share of the per-tile chain;
 //   warps 4-7 producer: the tile's 9 chunks of 128 rows by 16-byte cp.async
 //   into the 128-byte swizzled layout, 8 consecutive threads per 128-byte
 //   row chunk (rows of 1152 bytes anywhere in the pool); the tile stays
@@ -39,7 +41,7 @@
 //   soon as its last MMA is done (chunk 8 right after QK, chunks 0-7 after
 //   their PV block);
 //   warp 8 TMEM owner and MMA issuer; warp 9 streams Q's chunks from L2 by
-//   TMA through a three-slot ring.
+//   TMA through a five-slot ring.
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
@@ -60,7 +62,8 @@ constexpr int kChunkBytes = kRows * 128;     // 64 dims x 128 rows, bf16
 constexpr int kQRing = 5;                    // Q chunks in flight
 constexpr int kQChunkBytes = kHq * 128;      // 8 KB
 constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
-constexpr int kThreads = 320;                // 4 softmax + 4 producer + MMA + Q loader warps
+constexpr int kThreads = 448;         // softmax 0-3 + 10-13, producer 4-7, MMA 8, Q loader 9
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
 constexpr uint32_t kColO = 128;  // four 64-column O^T blocks
@@ -292,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.sfull[i], 1);
-      mbar_init(&sm.sempty[i], 128);
+      mbar_init(&sm.sempty[i], kSoftmaxThreads);
     }
-    mbar_init(&sm.pfull, 128);
+    mbar_init(&sm.pfull, kSoftmaxThreads);
     mbar_init(&sm.pempty, 1);
     mbar_init(&sm.ofull, 1);
-    mbar_init(&sm.ofree, 128);
-    mbar_init(&sm.smsync, 128);
+    mbar_init(&sm.ofree, kSoftmaxThreads);
+    mbar_init(&sm.smsync, kSoftmaxThreads);
     mbar_init(&sm.prsync, 128);
     mbar_init(&sm.done, 1);
     fence_mbar_init();
@@ -460,10 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------- softmax + finalize --
     // Thread = TMEM lane = row of the tile (and dv lane of O at the end).
-    // The loops over 32-column groups stay rolled: this code runs once per
-    // tile, so it has to stay small enough to be fetched quickly.
-    const int row = threadIdx.x;
-    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    // Two warps per TMEM lane quadrant: warps 0-3 take the heads 0-31 (the
+    // first 32 columns of S and of each O block), warps 10-13 heads 32-63.
+    const int quad = warp & 3;
+    const int half = warp >= 10 ? 1 : 0;
+    const int row = quad * 32 + lane;
+    const uint32_t lanes = (uint32_t)(quad * 32) << 16;
     const float c = a.scale_log2;
     int u = 0, sa = 0;
     uint32_t sp = 0;
@@ -476,9 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = a.out + (size_t)r * kHq * kDv;
       if (s.active() == 0) {
         if (s.complete) {
-          for (int i = row; i < kHq * kDv; i += 128) out[i] = __float2bfloat16(0.0f);
-          if (a.lse && row < kHq) a.lse[(size_t)r * kHq + row] = -INFINITY;
-        } else if (row < kHq) {
+          for (int i = row + 128 * half; i < kHq * kDv; i += 256) out[i] = __float2bfloat16(0.0f);
+          if (a.lse && half == 0 && row < kHq) a.lse[(size_t)r * kHq + row] = -INFINITY;
+        } else if (half == 0 && row < kHq) {
           pml[2 * row] = -INFINITY;
           pml[2 * row + 1] = 0.0f;
         }
@@ -492,21 +497,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ta = tbase + lanes + kColS + 64 * (u & 1);
-        // pass 1: per-head maximum of the tile
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+        // pass 1: per-head maximum of the tile (this warp's 32 heads)
+        {
           uint32_t raw[32];
           tmem_ld_32cols(ta + 32 * half, raw);
           tmem_wait_ld();
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
-          sm.redm[warp][32 * half + lane] = butterfly32<true>(v, lane);
+          sm.redm[quad][32 * half + lane] = butterfly32<true>(v, lane);
         }
         if (t + 1 < s.act_end)
           valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        if (row < kHq) {
+        if (half == 0 && row < kHq) {
           // thread h owns head h: the previous tile's sums, then the new max
           const int h = row;
           if (pend_l)
@@ -528,13 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
         const bool resc = sm.rescale[u & 1] != 0;
-        if (row == 0) sm.rescale[(u + 1) & 1] = 0;
+        if (half == 0 && row == 0) sm.rescale[(u + 1) & 1] = 0;
         // the previous PV must be done before P^T (and, if needed, O) change
         if (!warp_wait(&sm.pempty, (u & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         if (resc) {
 #pragma unroll 1
-          for (int q = 0; q < 8; ++q) {
+          for (int q = half; q < 8; q += 2) {
             const uint32_t to = tbase + lanes + kColO + 64 * (q >> 1) + 32 * (q & 1);
             uint32_t raw[32];
             tmem_ld_32cols(to, raw);
@@ -551,8 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool split = s.n <= kSplitRows;
         uint8_t* rh = sm.phi + row * 128;
         uint8_t* rl = sm.plo + row * 128;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+        {
           uint32_t raw[32];
           tmem_ld_32cols(ta + 32 * half, raw);
           tmem_wait_ld();
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(rl + off) =
                   make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
           }
-          sm.reds[warp][32 * half + lane] = butterfly32<false>(v, lane);
+          sm.reds[quad][32 * half + lane] = butterfly32<false>(v, lane);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- finalize the query segment: O out of TMEM ----
       if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // last tile's sums
-      if (row < kHq) {
+      if (half == 0 && row < kHq) {
         const int h = row;
         const float l = sm.l_run[h] * sm.fscale[h] +
                         ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
@@ -605,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&sm.ofull, sa & 1, &sm.abort)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int q = 0; q < 8; ++q) {
-        const int blk = q >> 1, half = q & 1;
+      for (int q = half; q < 8; q += 2) {
+        const int blk = q >> 1;
         uint32_t raw[32];
         tmem_ld_32cols(tbase + lanes + kColO + 64 * blk + 32 * half, raw);
         tmem_wait_ld();
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[(size_t)i * kDv] = __uint_as_float(raw[i]);
         }
       }
-      if (row < kHq) {
+      if (half == 0 && row < kHq) {
         const float m = sm.m_used[row], l = sm.l_run[row];
         if (s.complete) {
           if (a.lse)
@@ -636,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&sm.ofree);
       if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // stats read
-      if (row < kHq) {
+      if (half == 0 && row < kHq) {
         sm.m_used[row] = -INFINITY;
         sm.l_run[row] = 0.0f;
         sm.fscale[row] = 1.0f;
