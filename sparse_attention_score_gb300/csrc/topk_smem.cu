@@ -7,19 +7,24 @@
 // Ultra-Large-Scale MoE Models on Heterogeneous AI Accelerators", section 4:
 // equal scores resolve deterministically (the lower position wins).
 //
-// A row of n scores is cut into blocks of at most kCap positions.
+// A row of n scores is cut into as few blocks of at most kCap positions as
+// hold it.  (Cutting short rows further, to spread 32 decode rows over more
+// SMs, measured slower: 35 us against 21 us for rows of up to 32 K.)
 //   block step  : one CTA loads its block as order-preserving 32-bit keys into
 //                 shared memory and finds the exact K-th largest key T of the
-//                 block by three radix histograms (11 + 11 + 10 bits), all in
-//                 shared memory; the quota of keys equal to T is taken in
-//                 position order.  Kept positions are written in ascending
-//                 order by warp segments with one block-wide prefix.
+//                 block by radix histograms of up to 11 bits, all in shared
+//                 memory; the quota of keys equal to T is taken in position
+//                 order.  Kept positions are written in ascending order by
+//                 warp segments with one block-wide prefix.
 //   merge step  : when a row spans several blocks, the union of the blocks'
-//                 winners (which contains the row's exact top-K: anything that
-//                 beats a global winner inside its own block beats it
-//                 globally) is selected again by the same code, reading the
-//                 keys from the workspace.
-// Rows of at most kCap positions need one launch; longer rows two.
+//                 winners contains the row's exact top-K (anything that beats
+//                 a global winner inside its own block beats it globally).
+//                 Each block also stores its own K-th largest key; the row's
+//                 K-th largest key is at least the largest of those, B, so
+//                 only winners >= B take part.  A second kernel (one CTA per
+//                 row) selects again over them in shared memory and writes
+//                 the positions in block order, which is position order.
+// A row that fits one block takes one launch; other rows two.
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
 
@@ -33,13 +38,16 @@ constexpr int kCap = 49152;  // keys per CTA in shared memory (192 KB)
 
 constexpr int kWords = kCap / 32;  // one bit per key
 
+constexpr int kMaxBlocks = 32;  // blocks per row
+
 struct Shared {
   int hist[2048];
   uint32_t gtm[kWords], eqm[kWords];  // per 32 keys: which are > T, which == T
   uint32_t scan[kWarps + 1];
   int wgt[kWarps], weq[kWarps];
   int sel_bin, sel_above;
-  int chunk_off[33];
+  uint32_t bound;  // merge: the row's bound on its K-th largest key
+  int fcnt;
 };
 
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
@@ -265,19 +273,96 @@ __device__ __forceinline__ void emit(const uint32_t* keys, int cnt, uint32_t T, 
   }
 }
 
-// mode 0: block step writing final indices (row fits one block)
-// mode 1: block step writing the block's winners to the workspace
-// mode 2: merge step over a row's block winners
+// Merge of row r's block winners (one CTA per row).  The winners sit in the
+// workspace as [block][K] slots; they are loaded into shared memory in that
+// layout, each key raised by one, with 0 in the slots that hold nothing or a
+// key below the row's bound, so that every winner outranks every empty slot.
+// The selection and the ordered write are then those of the block step, over
+// slot indices: block order, then position order within a block, which is
+// ascending position order.
+__global__ void __launch_bounds__(kThreads, 1)
+    k_topk_merge(TopkParams a, int nchunks, const uint32_t* cand_key, const int32_t* cand_pos,
+                 const int* cand_cnt, const uint32_t* cand_kth) {
+  extern __shared__ uint4 keys_raw[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(keys_raw);
+  __shared__ Shared sh;
+  __shared__ int s_cnt[kMaxBlocks];
+  grid_dependency_wait();
+  launch_dependents();
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = a.K;
+  const long long base = (long long)r * nchunks * K;
+  if (warp == 0) {
+    uint32_t b = 0u;
+    int m = 0;
+    if (lane < nchunks) {
+      b = __ldg(&cand_kth[(long long)r * nchunks + lane]);
+      m = __ldg(&cand_cnt[(long long)r * nchunks + lane]);
+      s_cnt[lane] = m;
+    }
+    b = __reduce_max_sync(0xffffffffu, b);
+    if (lane == 0) sh.bound = b;
+  }
+  __syncthreads();
+  const uint32_t bound = sh.bound;
+  const int total = nchunks * K;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  int real = 0;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    const int j = i / K, q = i - j * K;
+    uint32_t k = 0u;
+    if (q < s_cnt[j]) {
+      const uint32_t v = __ldg(&cand_key[base + i]);
+      if (v >= bound) {
+        k = v + 1u;  // keys stay below 2^32 - 1: the largest is that of +inf
+        ++real;
+      }
+    }
+    keys[i] = k;
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  // number of winners >= bound (a block-wide sum through the scan buffer)
+  real = __reduce_add_sync(0xffffffffu, real);
+  if (lane == 0) sh.scan[warp] = (uint32_t)real;
+  block_min_max(kmin, kmax, sh);  // includes the barrier after the loads
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < kWarps; ++w) t += (int)sh.scan[w];
+    sh.fcnt = t;
+  }
+  __syncthreads();
+  const int fcnt = sh.fcnt;
+  const int keep_n = fcnt < K ? fcnt : K;
+  uint32_t T = 0u;  // every non-empty slot holds a key > 0
+  int need = 0;
+  if (keep_n < fcnt) {
+    need = keep_n;
+    select_threshold(keys, total, kmin, kmax, T, need, sh);
+  }
+  int32_t* out = a.idx + (long long)r * K;
+  emit(keys, total, T, need, false, out, (uint32_t*)nullptr,
+       [&](int i) { return __ldg(&cand_pos[base + i]); }, sh);
+  for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
+}
+
+// mode 0: the row is one block; writes the final indices
+// mode 1: block `blockIdx.x` of `nchunks` blocks of `blk` positions; writes
+//         the block's winners, their count and the block's K-th largest key
+//         (0 when the block has fewer than K positions) to the workspace
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
-    k_topk_block(TopkParams a, int nchunks, uint32_t* cand_key, int32_t* cand_pos, int* cand_cnt) {
+    k_topk_block(TopkParams a, int nchunks, int blk, uint32_t* cand_key, int32_t* cand_pos,
+                 int* cand_cnt, uint32_t* cand_kth) {
   extern __shared__ uint4 keys_raw[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(keys_raw);
   __shared__ Shared sh;
   grid_dependency_wait();
   launch_dependents();
-  const int r = kMode == 2 ? blockIdx.x : blockIdx.y;
-  const int c = kMode == 2 ? 0 : blockIdx.x;
+  const int r = blockIdx.y;
+  const int c = blockIdx.x;
   long long n = __ldg(&a.n_elig[r]);
   if (n < 0) n = 0;
   if (n > a.ld) {
@@ -285,13 +370,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     n = a.ld;
   }
   const int K = a.K;
-  int cnt;
-  long long start = 0;
+  const long long start = (long long)c * blk;
+  const long long rem = n - start;
+  const int cnt = (int)(rem < 0 ? 0 : (rem > blk ? blk : rem));
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  if (kMode != 2) {
-    start = (long long)c * kCap;
-    const long long rem = n - start;
-    cnt = (int)(rem < 0 ? 0 : (rem > kCap ? kCap : rem));
+  {
     const float* src = a.scores + (long long)r * a.ld + start;
     if ((((uintptr_t)src) & 15u) == 0) {
       // the whole block in flight at once (16-byte copies), then the scores
@@ -330,28 +413,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         kmax = max(kmax, k);
       }
     }
-  } else {
-    if (threadIdx.x == 0) {
-      int off = 0;
-      for (int j = 0; j < nchunks; ++j) {
-        sh.chunk_off[j] = off;
-        off += __ldg(&cand_cnt[(long long)r * nchunks + j]);
-      }
-      sh.chunk_off[nchunks] = off;
-    }
-    __syncthreads();
-    cnt = sh.chunk_off[nchunks];
-    for (int j = 0; j < nchunks; ++j) {
-      const int o = sh.chunk_off[j], m = sh.chunk_off[j + 1] - o;
-      const uint32_t* src = cand_key + ((long long)r * nchunks + j) * K;
-#pragma unroll 4
-      for (int i = threadIdx.x; i < m; i += kThreads) {
-        const uint32_t k = __ldg(&src[i]);
-        keys[o + i] = k;
-        kmin = min(kmin, k);
-        kmax = max(kmax, k);
-      }
-    }
   }
   block_min_max(kmin, kmax, sh);  // includes the barrier after the loads
 
@@ -366,22 +427,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     emit(keys, cnt, T, need, take_all, out, (uint32_t*)nullptr,
          [&](int i) { return (int32_t)(start + i); }, sh);
     for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
-  } else if (kMode == 1) {
+  } else {
     const long long slot = (long long)r * nchunks + c;
     emit(keys, cnt, T, need, take_all, cand_pos + slot * K, cand_key + slot * K,
          [&](int i) { return (int32_t)(start + i); }, sh);
-    if (threadIdx.x == 0) cand_cnt[slot] = keep_n;
-  } else {
-    int32_t* out = a.idx + (long long)r * K;
-    const int32_t* cp = cand_pos + (long long)r * nchunks * K;
-    emit(keys, cnt, T, need, take_all, out, (uint32_t*)nullptr,
-         [&](int i) {
-           int j = 0;
-           while (j + 1 < nchunks && sh.chunk_off[j + 1] <= i) ++j;
-           return __ldg(&cp[(long long)j * K + (i - sh.chunk_off[j])]);
-         },
-         sh);
-    for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
+    if (threadIdx.x == 0) {
+      cand_cnt[slot] = keep_n;
+      cand_kth[slot] = cnt >= K ? (take_all ? kmin : T) : 0u;
+    }
   }
 }
 
@@ -401,43 +454,58 @@ int topk_chunks(long long ld) { return (int)((ld + kCap - 1) / kCap); }
 
 bool topk_smem_eligible(long long ld, int K) {
   const int nch = topk_chunks(ld);
-  return nch <= 32 && (nch == 1 || (long long)nch * K <= kCap);
+  return nch <= kMaxBlocks && (nch == 1 || (long long)nch * K <= kCap);
 }
 
 size_t topk_smem_ws(int Nq, long long ld, int K) {
   const int nch = topk_chunks(ld);
   if (nch <= 1) return 0;
-  return (size_t)Nq * nch * ((size_t)K * 8 + 4) + 256;
+  // winners' keys and positions [Nq][nch][K], then counts and K-th keys [Nq][nch]
+  const size_t nslot = (size_t)Nq * nch;
+  return nslot * (size_t)K * 8 + nslot * 8 + 256;
 }
 
 int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   const int nch = topk_chunks(p.ld);
-  const size_t smem = (kCap + 4) * sizeof(uint32_t);
   if (nch == 1) {
     // a row shorter than the cap needs only its own keys in shared memory,
     // so that two CTAs (two rows) share an SM
     set_smem_attr<0>();
     const size_t smem0 = (size_t)((p.ld + 4 + 3) & ~3LL) * sizeof(uint32_t);
-    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem0, s, p, 1,
-                                     (uint32_t*)nullptr, (int32_t*)nullptr, (int*)nullptr);
+    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem0, s, p,
+                                     1, (int)p.ld, (uint32_t*)nullptr, (int32_t*)nullptr,
+                                     (int*)nullptr, (uint32_t*)nullptr);
     count_launch();
     if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
     return check_launch("topk");
   }
+  // block length: a multiple of 4 keys, so that blocks of a 16-byte aligned
+  // row start 16-byte aligned
+  const long long blk = ((p.ld + nch - 1) / nch + 3) & ~3LL;
   char* base = (char*)ws + kWsHeader;
   const size_t nslot = (size_t)p.Nq * nch;
   uint32_t* ckey = reinterpret_cast<uint32_t*>(base);
   int32_t* cpos = reinterpret_cast<int32_t*>(base + nslot * p.K * 4);
   int* ccnt = reinterpret_cast<int*>(base + nslot * p.K * 8);
+  uint32_t* ckth = reinterpret_cast<uint32_t*>(ccnt + nslot);
   set_smem_attr<1>();
-  set_smem_attr<2>();
-  cudaError_t e = launch_pdl(k_topk_block<1>, dim3(nch, p.Nq), dim3(kThreads), smem, s, p, nch,
-                             ckey, cpos, ccnt);
+  cudaError_t e = launch_pdl(k_topk_block<1>, dim3(nch, p.Nq), dim3(kThreads),
+                             (size_t)(blk + 4) * sizeof(uint32_t), s, p, nch, (int)blk, ckey, cpos,
+                             ccnt, ckth);
   count_launch();
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   int rc = check_launch("topk (blocks)");
   if (rc) return rc;
-  e = launch_pdl(k_topk_block<2>, dim3(p.Nq), dim3(kThreads), smem, s, p, nch, ckey, cpos, ccnt);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(k_topk_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (kCap + 4) * (int)sizeof(uint32_t));
+    attr = true;
+  }
+  e = launch_pdl(k_topk_merge, dim3(p.Nq), dim3(kThreads),
+                 (size_t)((long long)nch * p.K + 4) * sizeof(uint32_t), s, p, nch,
+                 (const uint32_t*)ckey, (const int32_t*)cpos, (const int*)ccnt,
+                 (const uint32_t*)ckth);
   count_launch();
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("topk (merge)");
