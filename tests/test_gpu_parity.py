@@ -263,6 +263,47 @@ def test_topk_long_rows_ties_across_blocks(K):
     assert dsa.get_status(ws) == 0
 
 
+def test_topk_long_rows_short_rows_and_special_values():
+    """The block + merge path on rows that leave blocks empty or short: no
+    eligible position, fewer than K (then no block bounds the merge), exactly
+    K across a block boundary, NaN (ranks below every value), -inf and -0
+    against +0, and winners only in the last block.  ld is odd, so every row
+    after the first starts off a 16-byte boundary."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(4242)
+    Nq, ld, K = 8, 100003, 2048
+    s = rng.integers(0, 3, size=(Nq, ld)).astype(np.float32)
+    s[2, ::7] = np.nan
+    s[3, ::5] = -np.inf
+    s[3, 1::5] = -0.0
+    s[4, :] = np.nan
+    s[4, 5000:5010] = 1.0
+    s[5, :] = -0.0
+    s[5, 1::2] = 0.0
+    s[6, 90000:] = 7.0
+    n = np.array([0, 100, 1500, ld, 40000, 60000, ld, K], np.int32)
+    st, ne = torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda()
+    idx = torch.empty((Nq, K), dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(dsa.topk_workspace_size(Nq, ld, K))
+    dsa.topk(st, ne, K, idx, ws)
+    got = idx.cpu().numpy()
+    # NaN ranks below every value: in rows without -inf a finite score below
+    # all others orders the same, and the oracle takes only numbers
+    ref = oracle.topk(np.where(np.isnan(s), np.float32(-1e30), s), n, K)
+    np.testing.assert_array_equal(got, ref)
+    assert dsa.get_status(ws) == 0
+    # the same workspace again, after a call of another shape left data in it
+    s2 = rng.standard_normal((3, 70001)).astype(np.float32)
+    n2 = np.array([70001, 33, 50000], np.int32)
+    idx2 = torch.empty((3, 512), dtype=torch.int32, device="cuda")
+    ws2 = dsa.workspace(max(dsa.topk_workspace_size(3, 70001, 512), ws.numel()))
+    dsa.topk(torch.from_numpy(s2).cuda(), torch.from_numpy(n2).cuda(), 512, idx2, ws2)
+    dsa.topk(st, ne, K, idx, ws2)
+    np.testing.assert_array_equal(idx2.cpu().numpy(), oracle.topk(s2, n2, 512))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("ld,K", [(20000, 2048), (65536, 4096), (4097, 7)])
 def test_topk_single_block_rows_ties_and_edges(ld, K):
     """Rows of 4K..64K positions (one shared-memory block each): heavy ties,
