@@ -5,8 +5,8 @@
  *   1. indexer score  -- "Day-0 Adaptation of Trillion-Parameter MoE Models on
  *      Domestic GPUs", section 3 (1) Index Selection: a lightweight similarity
  *      score of every cached position against the query;
- *   2. top-K          -- same passage ("block-wise scoring + intra-block
- *      reduction + cross-block merge"), with the deterministic tie rule of
+ *   2. top-K          -- same passage (the K best positions found block by
+ *      block, then combined across blocks), with the deterministic tie rule of
  *      "Day-0 Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
  *      Accelerators", section 4 (equal scores: the lower position wins);
  *   3. sparse attention -- first page, section 3 (3): exact softmax attention
@@ -91,7 +91,8 @@ typedef struct dsa_paged_layout {
 /* ---------------------------------------------------------------------------
  * Stage 1: indexer score.
  * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
- * section 3 (1) ("similarity scoring" of historical positions), read as
+ * section 3 (1) (each cached position scored by its similarity to the
+ * query through low-dimensional keys), read as
  *     scores[r][p] = sum_h w[r][h] * max(0, sum_d q_idx[r][h][d] * k_idx[p][d])
  * for every position p the query may see: p <= q_pos[r] and p < L_b (causal,
  * the current position included).  Entries of the row past the last eligible
@@ -138,8 +139,8 @@ int dsa_index_score_prefill(const dsa_paged_layout* layout, int seq, const void*
 /* ---------------------------------------------------------------------------
  * Stage 2: top-K selection.
  * Source: "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
- * section 3 (1) (Top-K filtering as block-wise scoring, intra-block reduction
- * and cross-block merge, without a global sort); tie rule from "Day-0
+ * section 3 (1) (selection done per block of positions and then combined
+ * over the blocks, with no sort of the whole row); tie rule from "Day-0
  * Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
  * Accelerators", section 4: among equal scores the lower position wins.
  * For row r, among positions 0..n_eligible[r]-1, keep the min(K, n) positions

@@ -13,7 +13,7 @@ cites the passage it follows:
   Domestic GPUs", section 3 (1) Index Selection ("similarity scoring", read as
   the ReLU-weighted sum over indexer heads of q_idx . k_idx), restricted to
   causal positions.
-* ``topk`` -- same page, section 3 (1) ("Top-K filtering"), with the tie rule
+* ``topk`` -- same page, section 3 (1) (the top-K selection), with the tie rule
   of "Day-0 Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI
   Accelerators", section 4 ("Determinism of index selection"): equal scores go
   to the lower position.

@@ -89,7 +89,7 @@ static int64_t or_phys_row(const int32_t* block_table, int max_blocks, int bs,
 }
 
 /* ---- stage 1: indexer score [P1 §3 (1); P2 §3.1 item 1] ----------------
- * "Similarity scoring" of every cached position against the query, read as
+ * Every cached position is scored by its similarity to the query, read as
  * the ReLU-weighted sum over indexer heads:
  *     s[r, p] = sum_h w[r, h] * max(0, sum_d q_idx[r, h, d] * k_idx[p, d])
  * for the positions p a query may attend to: p <= q_pos[r] and p < L_b
@@ -197,8 +197,8 @@ int oracle_topk(const float* scores, int64_t ld, const int32_t* n_elig, int Nq,
 }
 
 /* ---- stage 3: exact softmax attention over the selected rows -------------
- * [P1 §3 (3); P2 §3.1 item 3; P3 §4 execution chain "cache gather + sparse
- * attention"].  For query r (of sequence q_seq[r]) and head h, over the
+ * [P1 §3 (3); P2 §3.1 item 3; P3 §4 execution chain, the step that gathers
+ * the cached rows and attends over them].  For query r (of sequence q_seq[r]) and head h, over the
  * selected positions j (idx entries >= 0) whose rows are gathered through the
  * block table:
  *     z_j = sm_scale * sum_d q[r,h,d] * K[j,d]

@@ -2,8 +2,8 @@
 // per CTA held in shared memory.
 //
 // "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
-// section 3 (1): top-K as "block-wise scoring + intra-block reduction +
-// cross-block merge" without a global sort; "Day-0 Adaptation of
+// section 3 (1): the selection is made inside blocks of positions and the
+// blocks' results are then combined, with no sort of a whole row; "Day-0 Adaptation of
 // Ultra-Large-Scale MoE Models on Heterogeneous AI Accelerators", section 4:
 // equal scores resolve deterministically (the lower position wins).
 //
