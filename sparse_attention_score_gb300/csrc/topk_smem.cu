@@ -3,8 +3,9 @@
 //
 // "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
 // section 3 (1): the selection is made inside blocks of positions and the
-// blocks' results are then combined, with no sort of a whole row; "Day-0 Adaptation of
-// Ultra-Large-Scale MoE Models on Heterogeneous AI Accelerators", section 4:
+// blocks' results are then combined, with no sort of a whole row; "Day-0
+// Adaptation of Ultra-Large-Scale MoE Models on Heterogeneous AI Accelerators",
+// section 4:
 // equal scores resolve deterministically (the lower position wins).
 //
 // A row of n scores is cut into as few blocks of at most kCap positions as
@@ -38,7 +39,7 @@ constexpr int kCap = 49152;  // keys per CTA in shared memory (192 KB)
 
 constexpr int kWords = kCap / 32;  // one bit per key
 
-constexpr int kMaxBlocks = 32;  // blocks per row
+constexpr int kMaxBlocks = 32;  // blocks per row (the merge reads one bound per lane)
 
 struct Shared {
   int hist[2048];
