@@ -349,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
 }
 
+// Grid: x = row (up to 2^31 - 1 rows), y = block of the row.
 // mode 0: the row is one block; writes the final indices
-// mode 1: block `blockIdx.x` of `nchunks` blocks of `blk` positions; writes
+// mode 1: block `blockIdx.y` of `nchunks` blocks of `blk` positions; writes
 //         the block's winners, their count and the block's K-th largest key
 //         (0 when the block has fewer than K positions) to the workspace
 template <int kMode>
@@ -362,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ Shared sh;
   grid_dependency_wait();
   launch_dependents();
-  const int r = blockIdx.y;
-  const int c = blockIdx.x;
+  const int r = blockIdx.x;
+  const int c = blockIdx.y;
   long long n = __ldg(&a.n_elig[r]);
   if (n < 0) n = 0;
   if (n > a.ld) {
@@ -473,7 +474,7 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
     // so that two CTAs (two rows) share an SM
     set_smem_attr<0>();
     const size_t smem0 = (size_t)((p.ld + 4 + 3) & ~3LL) * sizeof(uint32_t);
-    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(1, p.Nq), dim3(kThreads), smem0, s, p,
+    const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(p.Nq, 1), dim3(kThreads), smem0, s, p,
                                      1, (int)p.ld, (uint32_t*)nullptr, (int32_t*)nullptr,
                                      (int*)nullptr, (uint32_t*)nullptr);
     count_launch();
@@ -490,7 +491,7 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   int* ccnt = reinterpret_cast<int*>(base + nslot * p.K * 8);
   uint32_t* ckth = reinterpret_cast<uint32_t*>(ccnt + nslot);
   set_smem_attr<1>();
-  cudaError_t e = launch_pdl(k_topk_block<1>, dim3(nch, p.Nq), dim3(kThreads),
+  cudaError_t e = launch_pdl(k_topk_block<1>, dim3(p.Nq, nch), dim3(kThreads),
                              (size_t)(blk + 4) * sizeof(uint32_t), s, p, nch, (int)blk, ckey, cpos,
                              ccnt, ckth);
   count_launch();

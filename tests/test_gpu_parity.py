@@ -304,6 +304,22 @@ def test_topk_long_rows_short_rows_and_special_values():
     np.testing.assert_array_equal(idx.cpu().numpy(), ref)
 
 
+def test_topk_more_rows_than_one_grid_dimension_holds():
+    """70,000 rows (one CTA each) exceed the 65,535 blocks of a grid's y and z
+    dimensions; the rows run on x."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(70000)
+    Nq, ld, K = 70000, 64, 8
+    s = rng.integers(0, 6, size=(Nq, ld)).astype(np.float32)
+    n = rng.integers(0, ld + 1, size=Nq).astype(np.int32)
+    idx = torch.empty((Nq, K), dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(dsa.topk_workspace_size(Nq, ld, K))
+    dsa.topk(torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda(), K, idx, ws)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle.topk(s, n, K))
+    assert dsa.get_status(ws) == 0
+
+
 @pytest.mark.parametrize("ld,K", [(20000, 2048), (65536, 4096), (4097, 7)])
 def test_topk_single_block_rows_ties_and_edges(ld, K):
     """Rows of 4K..64K positions (one shared-memory block each): heavy ties,
