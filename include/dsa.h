@@ -199,7 +199,10 @@ int dsa_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_eligible,
  *  k_pool       physical rows of Dqk bf16, k_row_stride elements apart
  *  v_pool       physical rows of Dv bf16, v_row_stride elements apart; may be
  *               k_pool itself (latent cache: V = first Dv dims of the K row)
- *  Hq           1..128 query heads; Dqk, Dv multiples of 8, <= 1024
+ *  Hq           1..64 query heads; Dqk, Dv multiples of 8 (>= 8), Dv <= 512,
+ *               Hq * Dqk * 2 + 4 * (Dqk + Dv) <= 200 KB (q of one query held in
+ *               shared memory); B (Nq for prefill) <= 65535.  Other shapes
+ *               return DSA_ERR_UNSUPPORTED.
  *  idx          [B][K] int32 positions from dsa_topk (-1 = padding, skipped)
  *  out          [B][Hq][Dv] bf16 output (0 for a row with no selected position)
  *  lse          [B][Hq] fp32 output, or NULL (-inf for an empty row)
