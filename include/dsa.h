@@ -112,8 +112,9 @@ typedef struct dsa_paged_layout {
  *  scores      [Nq][ld] fp32 output; ld >= eligible positions of every row
  *  ws          workspace of dsa_index_score_workspace_size() bytes
  * Errors: DSA_ERR_INVALID for null pointers, Nq < 0, ld < 1 or a bad layout;
- * DSA_ERR_UNSUPPORTED for other H_i/D_i/dtype.  Device: out-of-range block ids
- * give -inf scores and DSA_STATUS_BAD_BLOCK.
+ * DSA_ERR_UNSUPPORTED for other H_i/D_i/dtype and for Nq > 65535 (call in
+ * chunks of queries).  Device: out-of-range block ids give -inf scores and
+ * DSA_STATUS_BAD_BLOCK.
  */
 size_t dsa_index_score_workspace_size(int Nq, int H_i, int D_i, int64_t ld);
 int dsa_index_score(const dsa_paged_layout* layout, const void* q_idx, const float* w,
