@@ -586,9 +586,10 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": case.name, "queries_per_step_sampled": units / args.steps},
+        "config": config_of(case, world),
         "cpu_baseline": {"value": val, "unit": unit_of(case), "cores": 1, "kind": "oracle",
-                         "sample": f"{units} queries of {case.name} over {args.steps} steps"},
+                         "sample": f"{units} queries of {case.name} over {args.steps} steps "
+                                   f"({units / args.steps:.0f} per step)"},
         "e2e": {"value": val, "unit": unit_of(case), "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
