@@ -609,6 +609,40 @@ def config_of(case, world):
     return c
 
 
+def headline(args, world, res, peaks):
+    """The JSON line of the measured workload from run_gpu's result: whole-job
+    throughput (units of all ranks over the slowest rank's timed region), the
+    dominant kernel's roofline and, for decode, the whole path's."""
+    case = res["case"]
+    units = (case.Nq if case.kind == "prefill" else case.B) * world
+    value = units * args.steps / (res["total_ms"] / 1e3)
+    roof, step_work = roofline_of(res, peaks)
+    ms_step = res["total_ms"] / args.steps
+    line = {
+        "metric": metric_of(case), "value": value, "unit": unit_of(case), "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16+" + ("fp8" if case.idx_dtype == "fp8" else "bf16") + " (fp32 accumulate)",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": config_of(case, world),
+        "roofline": roof,
+        "stage_ms": {"index_score": res["stage_ms"][0], "topk": res["stage_ms"][1],
+                     "sparse_attn": res["stage_ms"][2]},
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
+        "gpu_launches_per_step": res["launches_per"],
+        "device_status": res["status"],
+        "cache_write": res["cache_write"],
+    }
+    if case.kind == "decode":
+        frac = step_work / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
+        line["path_roofline"] = {"bound": "hbm", "algorithmic_bytes_per_step": step_work,
+                                 "frac": round(frac, 4), "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s"}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -641,32 +675,7 @@ def main():
     res = run_gpu(args.workload, args.steps, args.warmup, rank, world, local_rank,
                   do_e2e=not args.no_e2e)
     case = res["case"]
-    units = (case.Nq if case.kind == "prefill" else case.B) * world
-    value = units * args.steps / (res["total_ms"] / 1e3)
-    roof, step_work = roofline_of(res, peaks)
-    ms_step = res["total_ms"] / args.steps
-    line = {
-        "metric": metric_of(case), "value": value, "unit": unit_of(case), "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16+" + ("fp8" if case.idx_dtype == "fp8" else "bf16") + " (fp32 accumulate)",
-        "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": config_of(case, world),
-        "roofline": roof,
-        "stage_ms": {"index_score": res["stage_ms"][0], "topk": res["stage_ms"][1],
-                     "sparse_attn": res["stage_ms"][2]},
-        "clocks": res["clocks"],
-        "e2e": res["e2e"],
-        "gpu_launches": res["launches"],
-        "gpu_launches_per_step": res["launches_per"],
-        "device_status": res["status"],
-        "cache_write": res["cache_write"],
-    }
-    if case.kind == "decode":
-        frac = step_work / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
-        line["path_roofline"] = {"bound": "hbm", "algorithmic_bytes_per_step": step_work,
-                                 "frac": round(frac, 4), "peak": peaks["hbm_gbs"],
-                                 "unit": "GB/s"}
+    line = headline(args, world, res, peaks)
     extra = [w for w in args.secondary.split(",") if w and w != args.workload]
     for wname in extra:
         r2 = run_gpu(wname, max(3, args.steps // 4), args.warmup, rank, world, local_rank,

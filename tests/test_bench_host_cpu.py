@@ -76,3 +76,38 @@ def test_roofline_takes_the_slower_stage_and_its_peak():
     assert roof["kernel"] == "index_score"
     assert roof["peak"] == pytest.approx(2 * 1877.6)
     assert roof["frac"] == pytest.approx(2.199e12 / 20e-3 / 1e12 / (2 * 1877.6), rel=1e-3)
+
+
+def test_headline_line_carries_the_contract_keys():
+    """The JSON line built from a (fake) measurement: every key the bench
+    contract names, whole-job throughput, and the roofline objects."""
+    c = _case("dec-batch", "decode", W.dec_batch_lens())
+    c.B, c.Nq, c.bs = 32, 32, 64
+    steps, total_ms = 20, 20 * 0.0861
+    res = {"case": c, "total_ms": total_ms, "stage_ms": [0.0233, 0.0210, 0.0533],
+           "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+           "e2e": {"value": 2.6e5, "unit": "queries/s", "h2d_bytes_per_step": 2694656,
+                   "d2h_bytes_per_step": 2097152},
+           "launches": 80, "launches_per": {"step": 4}, "status": 0, "cache_write": None}
+    args = types.SimpleNamespace(steps=steps, warmup=5)
+    for world in (1, 2):
+        line = bench.headline(args, world, res, PEAKS)
+        for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                  "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                  "roofline", "clocks", "e2e", "gpu_launches"):
+            assert k in line, k
+        assert line["metric"] == "decode queries/sec" and line["unit"] == "queries/s"
+        assert line["higher_is_better"] is True and line["scaling"] == "weak"
+        assert line["vs_baseline"] is None and line["n_gpus"] == world
+        # whole job: every rank's 32 queries over the slowest rank's time
+        assert line["value"] == pytest.approx(32 * world * steps / (total_ms / 1e3))
+        assert line["ms_per_step"] == pytest.approx(0.0861)
+        assert line["config"]["workload"] == "dec-batch"
+        assert line["config"]["parallelism"] == ("1gpu" if world == 1 else "replicas2")
+        assert "flushed" in line["config"]["l2"]
+        for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+            assert k in line["roofline"], k
+        for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+            assert k in line["e2e"], k
+        assert line["path_roofline"]["algorithmic_bytes_per_step"] == \
+            bench.algorithmic(c)["index_bytes"] + 75_497_472
