@@ -135,6 +135,47 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+class _Args:
+    """The operands of one call, checked so that no kernel can run outside
+    them: as each is added, its element size and element count (at least
+    what the call touches); then, in ptrs(), that every one of them and the
+    layout live on the GPU.  Sizes are checked for all operands before
+    residency for any, so that each check can be exercised with host
+    tensors."""
+
+    def __init__(self, layout: Optional["PagedLayout"] = None):
+        self._t = []
+        self._layout = layout
+
+    def add(self, t: Optional[torch.Tensor], name: str, elt=None, numel: Optional[int] = None):
+        if t is not None:
+            if elt is not None and t.element_size() not in elt:
+                raise TypeError(f"{name}: {t.dtype} has {t.element_size()}-byte elements; "
+                                f"the call needs {' or '.join(str(e) for e in elt)}")
+            if numel is not None and t.numel() < numel:
+                raise ValueError(f"{name}: {t.numel()} elements; the call needs at least "
+                                 f"{numel}")
+        self._t.append((t, name))
+        return self
+
+    def ptrs(self):
+        for t, name in self._t:
+            if t is not None and not t.is_cuda:
+                raise ValueError(f"{name}: a CUDA tensor is required")
+        lay = self._layout
+        if lay is not None and not (lay.block_table.is_cuda and lay.seq_lens.is_cuda):
+            raise ValueError("layout: block_table and seq_lens must be CUDA tensors")
+        return [_ptr(t) for t, _ in self._t]
+
+
+def _rows(layout: "PagedLayout", width: int) -> int:
+    """Elements of a paged pool of `width`-element rows."""
+    return int(layout.num_blocks) * int(layout.block_size) * int(width)
+
+
+_F32, _I32, _BF16, _KEY, _WS = (4,), (4,), (2,), (1, 2), (1,)  # element sizes (bytes)
+
+
 def _stream(stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -200,9 +241,14 @@ def index_score(layout: PagedLayout, q_idx, w, kidx_pool, scores, ws, q_seq=None
                 stream=None):
     """scores[Nq, ld] <- indexer scores (see include/dsa.h, dsa_index_score)."""
     Nq, H_i, D_i = q_idx.shape
-    rc = _lib.dsa_index_score(layout.c(), _ptr(q_idx), _ptr(w), _ptr(kidx_pool),
-                              _elt_dtype(kidx_pool), H_i, D_i, _ptr(q_seq), _ptr(q_pos), Nq,
-                              _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(), _stream(stream))
+    ld = scores.shape[1]
+    a = _Args(layout).add(q_idx, "q_idx", _KEY).add(w, "w", _F32, Nq * H_i)
+    a.add(kidx_pool, "kidx_pool", (q_idx.element_size(),), _rows(layout, D_i))
+    a.add(q_seq, "q_seq", _I32, Nq).add(q_pos, "q_pos", _I32, Nq)
+    a.add(scores, "scores", _F32, Nq * ld).add(ws, "ws", _WS)
+    pq, pw, pk, pseq, ppos, ps, pws = a.ptrs()
+    rc = _lib.dsa_index_score(layout.c(), pq, pw, pk, _elt_dtype(kidx_pool), H_i, D_i, pseq, ppos,
+                              Nq, ps, ld, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_index_score")
 
 
@@ -210,18 +256,24 @@ def index_score_prefill(layout: PagedLayout, seq, q_idx, w, kidx_pool, scores, w
                         stream=None):
     """scores[Nq, ld] <- indexer scores of Nq queries of sequence `seq`."""
     Nq, H_i, D_i = q_idx.shape
-    rc = _lib.dsa_index_score_prefill(layout.c(), int(seq), _ptr(q_idx), _ptr(w), _ptr(kidx_pool),
-                                      _elt_dtype(kidx_pool), H_i, D_i, _ptr(q_pos), Nq,
-                                      _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(),
-                                      _stream(stream))
+    ld = scores.shape[1]
+    a = _Args(layout).add(q_idx, "q_idx", _KEY).add(w, "w", _F32, Nq * H_i)
+    a.add(kidx_pool, "kidx_pool", (q_idx.element_size(),), _rows(layout, D_i))
+    a.add(q_pos, "q_pos", _I32, Nq).add(scores, "scores", _F32, Nq * ld).add(ws, "ws", _WS)
+    pq, pw, pk, ppos, ps, pws = a.ptrs()
+    rc = _lib.dsa_index_score_prefill(layout.c(), int(seq), pq, pw, pk, _elt_dtype(kidx_pool), H_i,
+                                      D_i, ppos, Nq, ps, ld, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_index_score_prefill")
 
 
 def topk(scores, n_eligible, K, idx, ws, stream=None):
     """idx[Nq, K] <- top-K positions, ascending, -1 padded."""
     Nq, ld = scores.shape
-    rc = _lib.dsa_topk(_ptr(scores), ld, _ptr(n_eligible), Nq, K, _ptr(idx), _ptr(ws), ws.numel(),
-                       _stream(stream))
+    K = int(K)
+    a = _Args().add(scores, "scores", _F32).add(n_eligible, "n_eligible", _I32, Nq)
+    a.add(idx, "idx", _I32, Nq * K).add(ws, "ws", _WS)
+    ps, pn, pi, pws = a.ptrs()
+    rc = _lib.dsa_topk(ps, ld, pn, Nq, K, pi, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_topk")
 
 
@@ -234,30 +286,42 @@ def topk_noalloc(scores, n_eligible, K, idx, stream=None):
     memory: the scratch is a fixed array inside the library, shared by every
     call (calls that overlap on the GPU race)."""
     Nq, ld = scores.shape
-    rc = _lib.dsa_topk_noalloc(_ptr(scores), ld, _ptr(n_eligible), Nq, K, _ptr(idx),
-                               _stream(stream))
+    K = int(K)
+    a = _Args().add(scores, "scores", _F32).add(n_eligible, "n_eligible", _I32, Nq)
+    a.add(idx, "idx", _I32, Nq * K)
+    ps, pn, pi = a.ptrs()
+    rc = _lib.dsa_topk_noalloc(ps, ld, pn, Nq, K, pi, _stream(stream))
     _check(rc, "dsa_topk_noalloc")
 
 
 def sparse_attn_decode(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
                        stream=None):
     B, Hq, Dqk = q.shape
-    Dv = out.shape[2]
-    rc = _lib.dsa_sparse_attn_decode(layout.c(), _ptr(q), _ptr(k_pool), k_pool.shape[-1],
-                                     _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(idx),
-                                     idx.shape[1], float(sm_scale), _ptr(out), _ptr(lse), _ptr(ws),
-                                     ws.numel(), _stream(stream))
+    Dv, K = out.shape[2], idx.shape[1]
+    ks, vs = k_pool.shape[-1], v_pool.shape[-1]
+    a = _Args(layout).add(q, "q", _BF16).add(k_pool, "k_pool", _BF16, _rows(layout, ks))
+    a.add(v_pool, "v_pool", _BF16, _rows(layout, vs)).add(idx, "idx", _I32, B * K)
+    a.add(out, "out", _BF16, B * Hq * Dv).add(lse, "lse", _F32, B * Hq)
+    a.add(ws, "ws", _WS)
+    pq, pk, pv, pi, po, pl, pws = a.ptrs()
+    rc = _lib.dsa_sparse_attn_decode(layout.c(), pq, pk, ks, pv, vs, Hq, Dqk, Dv, pi, K,
+                                     float(sm_scale), po, pl, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_sparse_attn_decode")
 
 
 def sparse_attn_prefill(layout: PagedLayout, q, k_pool, v_pool, idx, sm_scale, out, lse, ws,
                         q_seq=None, q_pos=None, stream=None):
     Nq, Hq, Dqk = q.shape
-    Dv = out.shape[2]
-    rc = _lib.dsa_sparse_attn_prefill(layout.c(), _ptr(q), _ptr(k_pool), k_pool.shape[-1],
-                                      _ptr(v_pool), v_pool.shape[-1], Hq, Dqk, Dv, _ptr(q_seq),
-                                      _ptr(q_pos), Nq, _ptr(idx), idx.shape[1], float(sm_scale),
-                                      _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    Dv, K = out.shape[2], idx.shape[1]
+    ks, vs = k_pool.shape[-1], v_pool.shape[-1]
+    a = _Args(layout).add(q, "q", _BF16).add(k_pool, "k_pool", _BF16, _rows(layout, ks))
+    a.add(v_pool, "v_pool", _BF16, _rows(layout, vs)).add(idx, "idx", _I32, Nq * K)
+    a.add(out, "out", _BF16, Nq * Hq * Dv).add(lse, "lse", _F32, Nq * Hq)
+    a.add(q_seq, "q_seq", _I32, Nq).add(q_pos, "q_pos", _I32, Nq).add(ws, "ws", _WS)
+    pq, pk, pv, pi, po, pl, pseq, ppos, pws = a.ptrs()
+    rc = _lib.dsa_sparse_attn_prefill(layout.c(), pq, pk, ks, pv, vs, Hq, Dqk, Dv, pseq, ppos, Nq,
+                                      pi, K, float(sm_scale), po, pl, pws, ws.numel(),
+                                      _stream(stream))
     _check(rc, "dsa_sparse_attn_prefill")
 
 
@@ -278,9 +342,16 @@ def cache_write(layout: PagedLayout, seq, pos, ws, kv_new=None, kv_pool=None, ki
     stride = int(kv_pool.shape[-1]) if kv_pool is not None else 0
     D_i = int(kidx_new.shape[-1]) if kidx_new is not None else 0
     kdt = _elt_dtype(kidx_new) if kidx_new is not None else DSA_BF16
-    rc = _lib.dsa_cache_write(layout.c(), _ptr(seq), _ptr(pos), N, _ptr(kv_new), row_elems,
-                              _ptr(kv_pool), stride, _ptr(kidx_new), D_i, kdt, _ptr(kidx_pool),
-                              _ptr(ws), ws.numel(), _stream(stream))
+    ke = (kidx_new.element_size(),) if kidx_new is not None else _KEY
+    a = _Args(layout).add(seq, "seq", _I32, N).add(pos, "pos", _I32, N)
+    a.add(kv_new, "kv_new", _BF16, N * row_elems)
+    a.add(kv_pool, "kv_pool", _BF16, _rows(layout, stride) if kv_new is not None else None)
+    a.add(kidx_new, "kidx_new", _KEY, N * D_i)
+    a.add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i) if kidx_new is not None else None)
+    a.add(ws, "ws", _WS)
+    pseq, ppos, pkv, pkp, pin, pip, pws = a.ptrs()
+    rc = _lib.dsa_cache_write(layout.c(), pseq, ppos, N, pkv, row_elems, pkp, stride, pin, D_i, kdt,
+                              pip, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_cache_write")
 
 
@@ -298,14 +369,23 @@ def decode_step(layout: PagedLayout, k_new, k_pool, kidx_new, kidx_pool, q_idx, 
     sequence's new K/V and indexer-key rows at position seq_lens[b] - 1, then
     score, select and attend.  v_pool None: V is the first Dv dims of the K row."""
     B, Hq, Dqk = q.shape
+    a = _Args(layout)
     H_i, D_i = q_idx.shape[1], q_idx.shape[2]
+    Dv, K, ld = out.shape[2], int(K), scores.shape[1]
     vp = k_pool if v_pool is None else v_pool
-    rc = _lib.dsa_decode_step(layout.c(), _ptr(k_new), _ptr(k_pool), k_pool.shape[-1], _ptr(v_new),
-                              _ptr(vp), vp.shape[-1], _ptr(kidx_new), _ptr(kidx_pool),
-                              _elt_dtype(kidx_pool), _ptr(q_idx), _ptr(w), H_i, D_i, _ptr(q), Hq,
-                              Dqk, out.shape[2], int(K), float(sm_scale), _ptr(scores),
-                              scores.shape[1], _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
-                              ws.numel(), _stream(stream))
+    ks, vs = k_pool.shape[-1], vp.shape[-1]
+    ke = (q_idx.element_size(),)
+    a.add(k_new, "k_new", _BF16, B * Dqk).add(k_pool, "k_pool", _BF16, _rows(layout, ks))
+    a.add(v_new, "v_new", _BF16, B * Dv).add(vp, "v_pool", _BF16, _rows(layout, vs))
+    a.add(kidx_new, "kidx_new", ke, B * D_i).add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i))
+    a.add(q_idx, "q_idx", _KEY).add(w, "w", _F32, B * H_i).add(q, "q", _BF16)
+    a.add(scores, "scores", _F32, B * ld).add(idx, "idx", _I32, B * K)
+    a.add(out, "out", _BF16, B * Hq * Dv).add(lse, "lse", _F32, B * Hq).add(ws, "ws", _WS)
+    (pkn, pkp, pvn, pvp, pin, pip, pqi, pw, pq, ps, pi, po, pl, pws) = a.ptrs()
+    rc = _lib.dsa_decode_step(layout.c(), pkn, pkp, ks, pvn, pvp, vs, pin, pip,
+                              _elt_dtype(kidx_pool), pqi, pw, H_i, D_i, pq, Hq, Dqk, Dv, K,
+                              float(sm_scale), ps, ld, pi, po, pl, pws, ws.numel(),
+                              _stream(stream))
     _check(rc, "dsa_decode_step")
 
 
@@ -316,21 +396,30 @@ def prefill_step(layout: PagedLayout, seq, q_pos, n_eligible, k_new, k_pool, kid
     call (include/dsa.h, dsa_prefill_step): its rows are written at q_pos, then
     scored, selected and attended."""
     Nq, Hq, Dqk = q.shape
+    a = _Args(layout).add(q_pos, "q_pos", _I32, Nq).add(n_eligible, "n_eligible", _I32, Nq)
     H_i, D_i = q_idx.shape[1], q_idx.shape[2]
+    Dv, K, ld = out.shape[2], int(K), scores.shape[1]
     vp = k_pool if v_pool is None else v_pool
-    rc = _lib.dsa_prefill_step(layout.c(), int(seq), _ptr(q_pos), _ptr(n_eligible), Nq,
-                               _ptr(k_new), _ptr(k_pool), k_pool.shape[-1], _ptr(v_new), _ptr(vp),
-                               vp.shape[-1], _ptr(kidx_new), _ptr(kidx_pool),
-                               _elt_dtype(kidx_pool), _ptr(q_idx), _ptr(w), H_i, D_i, _ptr(q), Hq,
-                               Dqk, out.shape[2], int(K), float(sm_scale), _ptr(scores),
-                               scores.shape[1], _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
-                               ws.numel(), _stream(stream))
+    ks, vs = k_pool.shape[-1], vp.shape[-1]
+    ke = (q_idx.element_size(),)
+    a.add(k_new, "k_new", _BF16, Nq * Dqk).add(k_pool, "k_pool", _BF16, _rows(layout, ks))
+    a.add(v_new, "v_new", _BF16, Nq * Dv).add(vp, "v_pool", _BF16, _rows(layout, vs))
+    a.add(kidx_new, "kidx_new", ke, Nq * D_i).add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i))
+    a.add(q_idx, "q_idx", _KEY).add(w, "w", _F32, Nq * H_i).add(q, "q", _BF16)
+    a.add(scores, "scores", _F32, Nq * ld).add(idx, "idx", _I32, Nq * K)
+    a.add(out, "out", _BF16, Nq * Hq * Dv).add(lse, "lse", _F32, Nq * Hq).add(ws, "ws", _WS)
+    (ppos, pn, pkn, pkp, pvn, pvp, pin, pip, pqi, pw, pq, ps, pi, po, pl, pws) = a.ptrs()
+    rc = _lib.dsa_prefill_step(layout.c(), int(seq), ppos, pn, Nq, pkn, pkp, ks, pvn, pvp, vs,
+                               pin, pip, _elt_dtype(kidx_pool), pqi, pw, H_i, D_i, pq, Hq, Dqk, Dv,
+                               K, float(sm_scale), ps, ld, pi, po, pl, pws, ws.numel(),
+                               _stream(stream))
     _check(rc, "dsa_prefill_step")
 
 
 def get_status(ws, clear: bool = True, stream=None) -> int:
     v = ctypes.c_int32(0)
-    _check(_lib.dsa_get_status(_ptr(ws), _stream(stream), ctypes.byref(v), int(clear)),
+    (pws,) = _Args().add(ws, "ws", _WS).ptrs()
+    _check(_lib.dsa_get_status(pws, _stream(stream), ctypes.byref(v), int(clear)),
            "dsa_get_status")
     return int(v.value)
 
