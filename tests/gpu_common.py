@@ -8,14 +8,42 @@ from workloads import device as wdev
 
 # Tolerances on attention outputs against the fp64 oracle (bf16 I/O, fp32
 # accumulation): max-abs 1e-2 and mean-abs 2e-3 on out; lse to 1e-3 absolute.
-# The output is stored as bf16, whose rounding alone moves a value by up to
-# 2^-9 of its magnitude (more than 1e-2 once |out| > 5.12, which a query with
-# a few selected rows reaches), so the max-abs bar applies to the error left
-# after that rounding: |gpu - ref| <= 1e-2 + 2^-9 |ref|.
+# The output is stored as bf16.  Only that store's own rounding is exempt from
+# the max-abs bar: an element passes when it is within 1e-2 of the exact
+# value, or within 1e-2 of the exact value rounded to bf16 (the nearest
+# representable output; the two differ only where the rounding alone moves a
+# value by more than 1e-2, i.e. |out| >= 4).  The mean-abs bar is taken
+# against the exact value.
 OUT_MAX_ABS = 1e-2
 OUT_MEAN_ABS = 2e-3
-BF16_HALF_ULP_REL = 2.0 ** -9
 LSE_ABS = 1e-3
+
+
+def bf16_nearest(x):
+    """float64 values rounded to the nearest bfloat16 value (ties to an even
+    significand), returned as float64.  Rounds once, from the float64 value:
+    the candidates are the bf16 neighbours of its float32 rounding, and the
+    nearest of them to x itself is taken."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    top = a.astype(np.float32).view(np.uint32).astype(np.int64) & 0xFFFF0000
+    cands = np.stack([np.maximum(top - 0x10000, 0), top, top + 0x10000])
+    vals = cands.astype(np.uint32).view(np.float32).astype(np.float64)
+    dist = np.abs(vals - a[None])
+    best = dist.min(axis=0)
+    # among the nearest candidates prefer the one with an even last bit
+    even = ((cands >> 16) & 1) == 0
+    score = np.where(dist == best[None], np.where(even, 0, 1), 2)
+    pick = np.take_along_axis(vals, score.argmin(axis=0)[None], axis=0)[0]
+    return np.copysign(pick, x)
+
+
+def out_errors(o, ref):
+    """Per-element error against the exact value, and whether each element
+    meets the max-abs bar with only the bf16 store's rounding exempt."""
+    err = np.abs(o - ref)
+    ok = (err <= OUT_MAX_ABS) | (np.abs(o - bf16_nearest(ref)) <= OUT_MAX_ABS)
+    return err, ok
 
 
 def need_gpu():
@@ -117,15 +145,19 @@ def assert_scores_equal(s_gpu, s_ref, n_elig):
 
 
 def assert_out_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
-    o = out_gpu.float().cpu().numpy().astype(np.float64)
-    err = np.abs(o - out_ref)
+    o = out_gpu.float().cpu().numpy().astype(np.float64) if hasattr(out_gpu, "cpu") else \
+        np.asarray(out_gpu, dtype=np.float64)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
-    excess = err - BF16_HALF_ULP_REL * np.abs(out_ref)
-    assert excess.max() <= OUT_MAX_ABS, (
-        f"{what}: max-abs {err.max():.3e} ({excess.max():.3e} beyond the bf16 store's rounding)")
+    err, ok = out_errors(o, out_ref)
+    if not ok.all():
+        bad = np.argwhere(~ok)[0]
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements beyond max-abs {OUT_MAX_ABS} "
+                             f"(first at {tuple(bad)}: gpu {o[tuple(bad)]!r}, "
+                             f"exact {out_ref[tuple(bad)]!r})")
     assert err.mean() <= OUT_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
     if lse_gpu is not None:
-        l = lse_gpu.cpu().numpy().astype(np.float64)
+        l = lse_gpu.cpu().numpy().astype(np.float64) if hasattr(lse_gpu, "cpu") else \
+            np.asarray(lse_gpu, dtype=np.float64)
         fin = np.isfinite(lse_ref)
         assert np.array_equal(np.isfinite(l), fin), f"{what}: lse finiteness differs"
         if fin.any():
