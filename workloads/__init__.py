@@ -58,7 +58,13 @@ _E4M3_OF_INT = _INT_VALUES.to(torch.float8_e4m3fn).view(torch.uint8).numpy().cop
 def encode_int(vals: np.ndarray, dtype: str) -> np.ndarray:
     """Encode integers in [-8, 8] as bf16 (uint16 bits) or E4M3 (uint8 bits)."""
     table = _BF16_OF_INT if dtype == "bf16" else _E4M3_OF_INT
-    return table[np.asarray(vals, dtype=np.int64) + 8]
+    vals = np.asarray(vals)
+    out = np.empty(vals.shape, dtype=table.dtype)
+    flat_in, flat_out = vals.reshape(-1), out.reshape(-1)
+    step = 1 << 26  # in slices, so that the index temporaries stay small
+    for s in range(0, flat_in.size, step):
+        flat_out[s:s + step] = table[flat_in[s:s + step].astype(np.int64) + 8]
+    return out
 
 
 def encode_bf16(x: np.ndarray) -> np.ndarray:
