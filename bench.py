@@ -411,18 +411,11 @@ def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
             "status": dsa.get_status(ws)}
 
 
-def run_e2e(case, d, pipe, steps, dev, flush):
-    """The same step end to end through the C ABI calls with host buffers:
-    H2D of the step's inputs (queries, indexer queries, weights, block table,
-    lengths) from pinned memory, the three stages, D2H of the attention
-    output, all inside the timed region.  The inputs travel as one packed
-    pinned buffer (one copy instead of five; the device tensors the stages
-    read are views into its device twin, captured in a graph of their own).
-    The paged KV and indexer-key caches are persistent device state and stay
-    resident."""
+def _e2e_inputs(case, dev):
+    """The step's inputs (queries, indexer queries, weights, block table,
+    lengths) as one packed pinned host buffer, its device twin, and views of
+    the twin shaped as each input (the stages read those)."""
     import torch
-
-    import sparse_attention_score_gb300 as dsa
     parts = {
         "q": (case.q, torch.bfloat16),
         "q_idx": (case.q_idx, torch.bfloat16 if case.idx_dtype == "bf16" else torch.uint8),
@@ -442,6 +435,25 @@ def run_e2e(case, d, pipe, steps, dev, flush):
     dbuf.copy_(hbuf)
     v = {k: dbuf[offs[k]:offs[k] + arr.nbytes].view(dt).view(arr.shape)
          for k, (arr, dt) in parts.items()}
+    return hbuf, dbuf, v, total
+
+
+def run_e2e(case, d, pipe, steps, dev, flush):
+    """The step end to end through the public API with host buffers, timed
+    two ways.  Every timed step holds: the H2D copy of the step's inputs from
+    pinned memory (one packed buffer), the three stages, and the D2H copy of
+    the attention output into pinned memory; the paged KV and indexer-key
+    caches are persistent device state and stay resident.  Before each step
+    L2 is flushed and the device synchronised, so host-side costs are not
+    hidden behind the flush.
+      calls : the three binding calls are made every step (ctypes marshalling,
+              operand checks and kernel launches inside the timed region);
+      graph : the three calls are captured once into a CUDA graph, replayed
+              each step."""
+    import torch
+
+    import sparse_attention_score_gb300 as dsa
+    hbuf, dbuf, v, total = _e2e_inputs(case, dev)
     layout = dsa.PagedLayout(v["block_table"], v["seq_lens"], case.bs, case.num_blocks,
                              case.max_len)
     out_host = torch.empty(pipe.out.shape, dtype=pipe.out.dtype).pin_memory()
@@ -469,28 +481,40 @@ def run_e2e(case, d, pipe, steps, dev, flush):
         stages()
     torch.cuda.synchronize()
 
-    def step():
+    def step_calls():
+        dbuf.copy_(hbuf, non_blocking=True)
+        stages()
+        out_host.copy_(pipe.out, non_blocking=True)
+
+    def step_graph():
         dbuf.copy_(hbuf, non_blocking=True)
         g.replay()
         out_host.copy_(pipe.out, non_blocking=True)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    tot = 0.0
-    for _ in range(steps):
-        flush(2.0)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step()
-        b.record(stream)
-        b.synchronize()
-        tot += a.elapsed_time(b)
     units = case.Nq if case.kind == "prefill" else case.B
-    return {"value": units * steps / (tot / 1e3), "unit": unit_of(case),
-            "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
-            "h2d_copies_per_step": 1, "d2h_copies_per_step": 1}
+    res = {}
+    for key, fn in (("calls", step_calls), ("graph", step_graph)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            flush(2.0)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        res[key] = {"value": units * steps / (tot / 1e3), "unit": unit_of(case),
+                    "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
+                    "h2d_copies_per_step": 1, "d2h_copies_per_step": 1}
+    res["calls"]["api"] = ("index_score, topk, sparse_attn called through the binding every "
+                           "step")
+    res["graph"]["api"] = "the same three calls captured once in a CUDA graph, replayed per step"
+    return res
 
 
 def unit_of(case):
@@ -561,11 +585,34 @@ def oracle_sample(case, budget_s=15.0, max_units=None):
     return done, time.perf_counter() - t0
 
 
+def host_cpu():
+    """The host the oracle runs on: logical CPUs and the CPU model (lscpu's
+    'Model name', else /proc/cpuinfo, else the platform string)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or
+            platform.machine()}
+
+
 def cpu_baseline(case, budget_s):
     n, t = oracle_sample(case, budget_s)
     return {"value": n / t, "unit": unit_of(case), "cores": 1, "kind": "oracle",
             "sample": f"{n} of {case.Nq} queries of {case.name} (all three stages, fp64 C oracle, "
-                      f"{t:.1f} s)"}
+                      f"{t:.1f} s)", "host": host_cpu()}
 
 
 def run_reference(args, rank, world):
@@ -589,7 +636,7 @@ def run_reference(args, rank, world):
         "config": config_of(case, world),
         "cpu_baseline": {"value": val, "unit": unit_of(case), "cores": 1, "kind": "oracle",
                          "sample": f"{units} queries of {case.name} over {args.steps} steps "
-                                   f"({units / args.steps:.0f} per step)"},
+                                   f"({units / args.steps:.0f} per step)", "host": host_cpu()},
         "e2e": {"value": val, "unit": unit_of(case), "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -629,18 +676,47 @@ def headline(args, world, res, peaks):
         "stage_ms": {"index_score": res["stage_ms"][0], "topk": res["stage_ms"][1],
                      "sparse_attn": res["stage_ms"][2]},
         "clocks": res["clocks"],
-        "e2e": res["e2e"],
+        "e2e": res["e2e"]["calls"] if res["e2e"] else None,
+        "e2e_graph": res["e2e"]["graph"] if res["e2e"] else None,
         "gpu_launches": res["launches"],
         "gpu_launches_per_step": res["launches_per"],
         "device_status": res["status"],
         "cache_write": res["cache_write"],
     }
-    if case.kind == "decode":
-        frac = step_work / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
-        line["path_roofline"] = {"bound": "hbm", "algorithmic_bytes_per_step": step_work,
-                                 "frac": round(frac, 4), "peak": peaks["hbm_gbs"],
-                                 "unit": "GB/s"}
+    line["path_roofline"] = path_roofline(case, ms_step, peaks)
     return line
+
+
+def path_roofline(case, ms_step, peaks):
+    """The whole step against its roofline: decode, the indexer keys plus the
+    gathered rows over HBM bandwidth; prefill, the ideal time of its tensor
+    work (FP8 indexer at twice the bf16 peak, bf16 attention) over the step."""
+    alg = algorithmic(case)
+    if case.kind == "decode":
+        step_bytes = alg["index_bytes"] + alg["gather_bytes"]
+        frac = step_bytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]
+        return {"bound": "hbm", "algorithmic_bytes_per_step": step_bytes, "frac": round(frac, 4),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    ideal_s = (alg["index_flops"] / (peaks["bf16_tflops"] * 2e12) +
+               alg["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
+    return {"bound": "tensor", "ideal_ms": round(ideal_s * 1e3, 4),
+            "frac": round(ideal_s / (ms_step / 1e3), 4)}
+
+
+def secondary_line(r2, st2, world, peaks):
+    """One more workload measured in the same run (same timing rules)."""
+    c2 = r2["case"]
+    u2 = (c2.Nq if c2.kind == "prefill" else c2.B) * world
+    roof2, _ = roofline_of(r2, peaks)
+    ms2 = r2["total_ms"] / st2
+    return {"metric": metric_of(c2), "value": u2 * st2 / (r2["total_ms"] / 1e3),
+            "unit": unit_of(c2), "ms_per_step": ms2, "steps": st2,
+            "config": config_of(c2, world), "roofline": roof2,
+            "path_roofline": path_roofline(c2, ms2, peaks),
+            "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
+            "gpu_launches": r2["launches"], "gpu_launches_per_step": r2["launches_per"],
+            "clocks": r2["clocks"], "device_status": r2["status"],
+            "cache_write": r2["cache_write"]}
 
 
 def main():
@@ -651,7 +727,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="dec-batch",
                     choices=["dec-tiny", "dec-batch", "prefill", "long-dec", "million"])
-    ap.add_argument("--secondary", default="prefill",
+    ap.add_argument("--secondary", default="prefill,dec-tiny,long-dec,million",
                     help="comma-separated extra workloads reported in the same line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
@@ -678,24 +754,9 @@ def main():
     line = headline(args, world, res, peaks)
     extra = [w for w in args.secondary.split(",") if w and w != args.workload]
     for wname in extra:
-        r2 = run_gpu(wname, max(3, args.steps // 4), args.warmup, rank, world, local_rank,
-                     do_e2e=False)
-        c2 = r2["case"]
-        u2 = (c2.Nq if c2.kind == "prefill" else c2.B) * world
         st2 = max(3, args.steps // 4)
-        roof2, work2 = roofline_of(r2, peaks)
-        sub = {"metric": metric_of(c2), "value": u2 * st2 / (r2["total_ms"] / 1e3),
-               "unit": unit_of(c2), "ms_per_step": r2["total_ms"] / st2, "steps": st2,
-               "config": config_of(c2, world), "roofline": roof2,
-               "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
-               "gpu_launches": r2["launches"], "clocks": r2["clocks"],
-               "cache_write": r2["cache_write"]}
-        if c2.kind == "prefill":
-            ideal_s = (algorithmic(c2)["index_flops"] / (peaks["bf16_tflops"] * 2e12) +
-                       algorithmic(c2)["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
-            sub["path_roofline"] = {"bound": "tensor", "frac": round(
-                ideal_s / (r2["total_ms"] / st2 / 1e3), 4)}
-        line[wname.replace("-", "_")] = sub
+        r2 = run_gpu(wname, st2, args.warmup, rank, world, local_rank, do_e2e=False)
+        line[wname.replace("-", "_")] = secondary_line(r2, st2, world, peaks)
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
     if rank == 0:

@@ -86,8 +86,8 @@ def test_headline_line_carries_the_contract_keys():
     steps, total_ms = 20, 20 * 0.0861
     res = {"case": c, "total_ms": total_ms, "stage_ms": [0.0233, 0.0210, 0.0533],
            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
-           "e2e": {"value": 2.6e5, "unit": "queries/s", "h2d_bytes_per_step": 2694656,
-                   "d2h_bytes_per_step": 2097152},
+           "e2e": {k: {"value": 2.6e5, "unit": "queries/s", "h2d_bytes_per_step": 2694656,
+                       "d2h_bytes_per_step": 2097152} for k in ("calls", "graph")},
            "launches": 80, "launches_per": {"step": 4}, "status": 0, "cache_write": None}
     args = types.SimpleNamespace(steps=steps, warmup=5)
     for world in (1, 2):
