@@ -170,8 +170,10 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
  *    library, present on every GPU that loads it until the process exits.  No
  *    call allocates or frees device memory.
  *  First call on a device: looks up the array's device address (once per
- *    device, with that device current).  Make that first call before any
- *    stream capture.
+ *    device, with that device current) and keeps it for the life of the
+ *    process.  Make that first call before any stream capture.  A
+ *    cudaDeviceReset() of that device invalidates the kept address: do not
+ *    reset a device between calls of this function in one process.
  *  Limit: a problem whose scratch would exceed the array
  *    (dsa_topk_workspace_size() > DSA_TOPK_NOALLOC_SCRATCH_BYTES) is rejected
  *    with DSA_ERR_WORKSPACE and a message; nothing is launched.
@@ -183,6 +185,10 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
 #define DSA_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
 int dsa_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq, int K,
                      int32_t* idx, dsa_stream_t stream);
+/* The size of that fixed array as this build of the library has it
+ * (DSA_TOPK_NOALLOC_SCRATCH_BYTES), for callers that load the library at run
+ * time and cannot see the header's define. */
+size_t dsa_topk_noalloc_scratch_bytes(void);
 
 /* ---------------------------------------------------------------------------
  * Stage 3a: sparse attention, decode (one query per sequence).

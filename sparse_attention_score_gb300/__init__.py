@@ -86,6 +86,7 @@ _sig("dsa_index_score_prefill", _i, [_LP, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _i
 _sig("dsa_topk_workspace_size", _sz, [_i, _i64, _i])
 _sig("dsa_topk", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_topk_noalloc", _i, [_vp, _i64, _vp, _i, _i, _vp, _vp])
+_sig("dsa_topk_noalloc_scratch_bytes", _sz, [])
 _sig("dsa_decode_step_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, _i, _i])
 _sig("dsa_decode_step", _i, [_LP, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i, _vp, _vp, _i, _i,
                              _vp, _i, _i, _i, _i, _f, _vp, _i64, _vp, _vp, _vp, _vp, _sz, _vp])
@@ -107,7 +108,8 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_index_score_workspace_size", "dsa_index_score",
            "dsa_index_score_prefill_workspace_size", "dsa_index_score_prefill",
            "dsa_topk_workspace_size",
-           "dsa_topk", "dsa_topk_noalloc", "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
+           "dsa_topk", "dsa_topk_noalloc", "dsa_topk_noalloc_scratch_bytes",
+           "dsa_sparse_attn_decode_workspace_size", "dsa_sparse_attn_decode",
            "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill",
            "dsa_cache_write_workspace_size", "dsa_cache_write",
            "dsa_decode_step_workspace_size", "dsa_decode_step",
@@ -277,8 +279,9 @@ def topk(scores, n_eligible, K, idx, ws, stream=None):
     _check(rc, "dsa_topk")
 
 
-# Size of the fixed scratch array dsa_topk_noalloc uses (DSA_TOPK_NOALLOC_SCRATCH_BYTES).
-TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
+# Size of the fixed scratch array dsa_topk_noalloc uses, as the loaded library
+# reports it (DSA_TOPK_NOALLOC_SCRATCH_BYTES in include/dsa.h).
+TOPK_NOALLOC_SCRATCH_BYTES = int(_lib.dsa_topk_noalloc_scratch_bytes())
 
 
 def topk_noalloc(scores, n_eligible, K, idx, stream=None):

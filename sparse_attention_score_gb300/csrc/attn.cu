@@ -196,11 +196,8 @@ template <int HPW, int DVL>
 int launch_generic(const AttnParams& p, cudaStream_t s) {
   auto kern = k_attn_generic<HPW, DVL>;
   const size_t smem = (size_t)p.Hq * p.Dqk * 2 + sizeof(float) * (p.Dqk + p.Dv);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set = true;
-  }
+  const int arc = ensure_dynamic_smem((const void*)kern, 200 * 1024, "sparse_attn");
+  if (arc) return arc;
   kern<<<dim3(p.S, p.Nq), kAttnThreads, smem, s>>>(p);
   count_launch();
   return check_launch("sparse_attn");

@@ -769,11 +769,8 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   float* part_ml = reinterpret_cast<float*>((char*)ws + kWsHeader);
   float* part_o = part_ml + (size_t)2 * kMaxCtas * kHq * 2;
   const size_t smem = sizeof(Smem) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
-  }
+  rc = ensure_dynamic_smem((const void*)k_attn_tc, (int)smem, "sparse_attn (tensor cores)");
+  if (rc) return rc;
   Geo g;
   g.Tq = (p.K + kRows - 1) / kRows;
   g.total = (long long)p.Nq * g.Tq;

@@ -108,7 +108,10 @@ int check_launch(const char* what);
 // apart; box of box_inner x box_rows.
 int make_tmap_2d(CUtensorMap* map, const void* base, bool one_byte, uint64_t inner_elems,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
-int sm_count();
+int sm_count();  // of the current device
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (once per kernel and device, thread-safe); DSA_ERR_CUDA on failure.
+int ensure_dynamic_smem(const void* kernel, int bytes, const char* what);
 
 // launchers: return DSA_OK / DSA_ERR_*
 int launch_index_score(const IndexParams& p, cudaStream_t s);

@@ -4,8 +4,10 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <map>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "dsa_internal.cuh"
 
@@ -43,14 +45,39 @@ int make_tmap_2d(CUtensorMap* map, const void* base, bool one_byte, uint64_t inn
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  static std::mutex m;
+  static std::map<int, int> counts;
+  std::lock_guard<std::mutex> lock(m);
+  auto it = counts.find(dev);
+  if (it != counts.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  counts[dev] = n;
   return n;
+}
+
+int ensure_dynamic_smem(const void* kernel, int bytes, const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return set_error(DSA_ERR_CUDA, std::string(what) + ": cudaGetDevice: " + cudaGetErrorString(e));
+  // function attributes belong to a device's context: one record per
+  // (kernel, device), the largest size set so far
+  static std::mutex m;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::mutex> lock(m);
+  const auto key = std::make_pair(kernel, dev);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return DSA_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess)
+    return set_error(DSA_ERR_CUDA, std::string(what) + ": cudaFuncSetAttribute(" +
+                                       std::to_string(bytes) + " bytes): " + cudaGetErrorString(e));
+  done[key] = bytes;
+  return DSA_OK;
 }
 
 }  // namespace dsa

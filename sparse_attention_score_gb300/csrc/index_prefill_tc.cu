@@ -354,11 +354,9 @@ int launch_index_prefill_tc(const IndexParams& p, cudaStream_t s) {
                     kGroupQ * kHeads);
   if (rc) return rc;
   const size_t smem = sizeof(Smem) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_index_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
-  }
+  rc = ensure_dynamic_smem((const void*)k_index_prefill_tc, (int)smem,
+                          "index_score prefill (tensor cores)");
+  if (rc) return rc;
   const long long nblocks = (p.Nq + kQB - 1) / kQB;
   const long long max_items = nblocks * ((p.ld + kTileRows - 1) / kTileRows);
   long long grid = sm_count();

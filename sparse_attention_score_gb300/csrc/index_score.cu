@@ -115,11 +115,8 @@ template <int D, int DT>
 int launch_generic(const IndexParams& p, cudaStream_t s) {
   const size_t smem = sizeof(float) * ((size_t)p.H * D + p.H);
   auto kern = k_index_score_generic<D, DT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    attr_set = true;
-  }
+  const int arc = ensure_dynamic_smem((const void*)kern, 96 * 1024, "index_score");
+  if (arc) return arc;
   dim3 grid((unsigned)((p.ld + kGenThreads - 1) / kGenThreads), (unsigned)p.Nq);
   kern<<<grid, kGenThreads, smem, s>>>(p);
   count_launch();

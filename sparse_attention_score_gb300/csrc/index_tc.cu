@@ -382,11 +382,8 @@ int launch_index_tc(const IndexParams& p, cudaStream_t s) {
                     kHeads);
   if (rc) return rc;
   const size_t smem = sizeof(Smem) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_index_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
-  }
+  rc = ensure_dynamic_smem((const void*)k_index_tc, (int)smem, "index_score (tensor cores)");
+  if (rc) return rc;
   const long long max_tiles = (long long)p.Nq * ((p.ld + kTileRows - 1) / kTileRows);
   long long grid = 2LL * sm_count();
   if (grid > max_tiles) grid = max_tiles;

@@ -33,7 +33,9 @@ std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device; the first call
-// on a device looks it up and caches it.
+// on a device looks it up and caches it for the life of the process (a
+// cudaDeviceReset of that device would leave the cached address stale, which
+// the header tells callers not to do between calls).
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -59,6 +61,8 @@ int scratch_address(void** out) {
 }  // namespace dsa
 
 using namespace dsa;
+
+extern "C" size_t dsa_topk_noalloc_scratch_bytes(void) { return sizeof(g_topk_scratch); }
 
 extern "C" int dsa_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_eligible,
                                 int Nq, int K, int32_t* idx, dsa_stream_t stream) {

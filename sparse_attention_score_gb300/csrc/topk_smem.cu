@@ -441,13 +441,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 template <int kMode>
-void set_smem_attr() {
-  static bool done = false;
-  if (!done) {
-    cudaFuncSetAttribute(k_topk_block<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (kCap + 4) * (int)sizeof(uint32_t));
-    done = true;
-  }
+int set_smem_attr() {
+  return ensure_dynamic_smem((const void*)k_topk_block<kMode>, (kCap + 4) * (int)sizeof(uint32_t),
+                             "topk");
 }
 
 }  // namespace
@@ -472,7 +468,8 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   if (nch == 1) {
     // a row shorter than the cap needs only its own keys in shared memory,
     // so that two CTAs (two rows) share an SM
-    set_smem_attr<0>();
+    const int arc = set_smem_attr<0>();
+    if (arc) return arc;
     const size_t smem0 = (size_t)((p.ld + 4 + 3) & ~3LL) * sizeof(uint32_t);
     const cudaError_t e = launch_pdl(k_topk_block<0>, dim3(p.Nq, 1), dim3(kThreads), smem0, s, p,
                                      1, (int)p.ld, (uint32_t*)nullptr, (int32_t*)nullptr,
@@ -490,20 +487,18 @@ int launch_topk_smem(const TopkParams& p, void* ws, cudaStream_t s) {
   int32_t* cpos = reinterpret_cast<int32_t*>(base + nslot * p.K * 4);
   int* ccnt = reinterpret_cast<int*>(base + nslot * p.K * 8);
   uint32_t* ckth = reinterpret_cast<uint32_t*>(ccnt + nslot);
-  set_smem_attr<1>();
+  int rc = set_smem_attr<1>();
+  if (rc) return rc;
   cudaError_t e = launch_pdl(k_topk_block<1>, dim3(p.Nq, nch), dim3(kThreads),
                              (size_t)(blk + 4) * sizeof(uint32_t), s, p, nch, (int)blk, ckey, cpos,
                              ccnt, ckth);
   count_launch();
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
-  int rc = check_launch("topk (blocks)");
+  rc = check_launch("topk (blocks)");
   if (rc) return rc;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_topk_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (kCap + 4) * (int)sizeof(uint32_t));
-    attr = true;
-  }
+  rc = ensure_dynamic_smem((const void*)k_topk_merge, (kCap + 4) * (int)sizeof(uint32_t),
+                           "topk (merge)");
+  if (rc) return rc;
   e = launch_pdl(k_topk_merge, dim3(p.Nq), dim3(kThreads),
                  (size_t)((long long)nch * p.K + 4) * sizeof(uint32_t), s, p, nch,
                  (const uint32_t*)ckey, (const int32_t*)cpos, (const int*)ccnt,

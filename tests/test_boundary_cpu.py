@@ -121,3 +121,14 @@ def test_attention_rejects_bad_arguments(dsa):
 def test_get_status_rejects_null(dsa):
     v = ctypes.c_int32(0)
     assert dsa.lib().dsa_get_status(None, None, ctypes.byref(v), 0) == -1
+
+
+def test_noalloc_scratch_size_matches_the_header(dsa):
+    """The binding's limit for dsa_topk_noalloc is the library's own (queried
+    through dsa_topk_noalloc_scratch_bytes), and equals the header's define."""
+    m = re.search(r"#define\s+DSA_TOPK_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)",
+                  open(HEADER).read())
+    assert m, "DSA_TOPK_NOALLOC_SCRATCH_BYTES not found in the header"
+    want = int(m.group(1)) << int(m.group(2))
+    assert int(dsa.lib().dsa_topk_noalloc_scratch_bytes()) == want
+    assert dsa.TOPK_NOALLOC_SCRATCH_BYTES == want

@@ -5,7 +5,7 @@ plugin given only a stream, a real-time thread that must not take allocator
 locks, a process whose device memory is divided up in advance): its scratch
 is one fixed array inside the library, reused by every call.  These tests
 check that it selects exactly what dsa_topk selects with a caller-owned
-workspace, on consecutive calls of different shapes (so that what one call
+workspace, and what the CPU oracle selects, on consecutive calls of different shapes (so that what one call
 leaves in the array cannot leak into the next), and that a problem too big
 for the array is refused before anything runs.
 
@@ -19,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_common import lib, need_gpu
 
 pytestmark = pytest.mark.gpu
@@ -70,6 +71,10 @@ def test_no_alloc_topk_matches_dsa_topk_on_consecutive_calls():
         got = _no_alloc(dsa, scores, n, K)
         torch.cuda.synchronize()
         assert torch.equal(got, want), (seed, Nq, ld, K)
+        # and both are the oracle's selection (full sort by score desc,
+        # position asc; ascending output, -1 padding)
+        ref = oracle.topk(scores.cpu().numpy(), n.cpu().numpy(), K)
+        np.testing.assert_array_equal(got.cpu().numpy(), ref, err_msg=str((seed, Nq, ld, K)))
 
 
 def test_no_alloc_topk_refuses_a_problem_beyond_its_scratch():
