@@ -22,18 +22,61 @@ namespace {
 
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kRowChunk = kAttnThreads;  // selected rows looked up per pass
+constexpr int kMaxTile = 32;             // rows per K/V tile (one per lane)
+constexpr int kSmemLimit = 227 * 1024;   // opt-in shared memory per CTA
+constexpr int kMaxSplits = 64;
 
-// grid (S, Nq); warp w owns heads w, w+8, ...; lane l owns dims l, l+32, ...
-template <int HPW, int DVL>
-__global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
+// 16-byte global -> shared copy; with ok false nothing is read and the
+// destination is zero-filled (the source must still be a valid address).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prev() {  // all groups but the newest done
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 u = __bfloat1622float2(x[i]), v = __bfloat1622float2(y[i]);
+    acc = fmaf(u.x, v.x, acc);
+    acc = fmaf(u.y, v.y, acc);
+  }
+  return acc;
+}
+
+// Shared memory of k_attn_generic for tiles of T rows.
+__host__ __device__ inline size_t generic_smem(int Hq, int Dqk, int Dv, int T) {
+  return (size_t)Hq * Dqk * 2 + (size_t)2 * T * ((Dqk + 8) + Dv) * 2 +
+         (size_t)kRowChunk * 8 + 2 * kMaxTile * 4;
+}
+
+// grid (S, Nq): CTA (split, r) takes its range of query r's selected rows in
+// tiles of T rows.  The page-table lookups of up to 256 rows run at once (one
+// thread per row); the K/V rows of tile t+1 are copied (cp.async) while tile
+// t is scored.  Warp w owns heads w, w+8, ...: in scoring lane t owns row t of
+// the tile, in the P.V product lane l owns output dims 2l, 2l+1, 2l+64, ...
+template <int HPW, int DVP>
+__global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a, int T) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int Hq = a.Hq, Dqk = a.Dqk, Dv = a.Dv;
+  const int KS = Dqk + 8;  // padded K row: 16-byte reads of consecutive rows hit distinct banks
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smraw);  // [Hq][Dqk]
+  __nv_bfloat16* ksm = qs + (size_t)Hq * Dqk;                   // [2][T][KS]
+  __nv_bfloat16* vsm = ksm + (size_t)2 * T * KS;                // [2][T][Dv]
+  long long* rows = reinterpret_cast<long long*>(vsm + (size_t)2 * T * Dv);  // [kRowChunk]
+  int* valid = reinterpret_cast<int*>(rows + kRowChunk);                     // [2][kMaxTile]
   grid_dependency_wait();
   launch_dependents();
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smraw);          // [Hq][Dqk]
-  float* krow = reinterpret_cast<float*>(smraw + (size_t)Hq * Dqk * 2);  // [Dqk]
-  float* vrow = krow + Dqk;                                               // [Dv]
-  __shared__ long long row_sh;
 
   const int r = blockIdx.y, split = blockIdx.x, S = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -44,15 +87,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
     reinterpret_cast<uint4*>(qs)[i] =
         __ldg(reinterpret_cast<const uint4*>(a.q + (long long)r * Hq * Dqk) + i);
 
-  float m[HPW], l[HPW], o[HPW][DVL];
-#pragma unroll
-  for (int i = 0; i < HPW; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < DVL; ++k) o[i][k] = 0.0f;
-  }
-
   const int per = (a.K + S - 1) / S;
   const int j0 = split * per, j1 = min(a.K, j0 + per);
   long long L = b_ok ? (long long)__ldg(&a.lay.seq_lens[b]) : 0;
@@ -60,9 +94,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
     const long long qp = (long long)__ldg(&a.q_pos[r]) + 1;  // positions <= q_pos
     if (qp < L) L = qp;
   }
-  for (int j = j0; j < j1; ++j) {
-    if (threadIdx.x == 0) {
-      long long row = -1;
+
+  // rows[t] = physical row of selected entry j0 + c * kRowChunk + t, or -1
+  auto lookup = [&](int c) {
+    const int j = j0 + c * kRowChunk + threadIdx.x;
+    long long row = -1;
+    if (j < j1) {
       const int p = __ldg(&a.idx[(long long)r * a.K + j]);
       if (!b_ok) {
         if (j == j0) flag_status(a.status, DSA_STATUS_BAD_INDEX);
@@ -74,70 +111,149 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a) {
           if (row < 0) flag_status(a.status, DSA_STATUS_BAD_BLOCK);
         }
       }
-      row_sh = row;
     }
-    __syncthreads();
-    const long long row = row_sh;
-    if (row < 0) {
-      __syncthreads();
-      continue;
+    rows[threadIdx.x] = row;
+  };
+  const int kp8 = Dqk >> 3, vp8 = Dv >> 3;
+  auto issue = [&](int tt) {
+    const int bb = tt & 1, base = (tt * T) % kRowChunk;
+    const int nt = min(T, j1 - (j0 + tt * T));
+    for (int i = threadIdx.x; i < T * kp8; i += kAttnThreads) {
+      const int t = i / kp8, c = i - t * kp8;
+      const long long row = t < nt ? rows[base + t] : -1;
+      cp_async16(ksm + ((size_t)bb * T + t) * KS + c * 8,
+                 row >= 0 ? a.kp + row * a.ks + c * 8 : a.kp, row >= 0);
     }
-    const __nv_bfloat16* kr = a.kp + row * a.ks;
-    const __nv_bfloat16* vr = a.vp + row * a.vs;
-    for (int d = threadIdx.x; d < Dqk; d += kAttnThreads) krow[d] = __bfloat162float(kr[d]);
-    for (int d = threadIdx.x; d < Dv; d += kAttnThreads) vrow[d] = __bfloat162float(vr[d]);
+    for (int i = threadIdx.x; i < T * vp8; i += kAttnThreads) {
+      const int t = i / vp8, c = i - t * vp8;
+      const long long row = t < nt ? rows[base + t] : -1;
+      cp_async16(vsm + ((size_t)bb * T + t) * Dv + c * 8,
+                 row >= 0 ? a.vp + row * a.vs + c * 8 : a.vp, row >= 0);
+    }
+    if (threadIdx.x < T)
+      valid[bb * kMaxTile + threadIdx.x] = threadIdx.x < nt && rows[base + threadIdx.x] >= 0;
+    cp_async_commit();
+  };
+
+  float m[HPW], l[HPW];
+  float2 o[HPW][DVP];
+#pragma unroll
+  for (int i = 0; i < HPW; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.0f;  // this lane's share of the sum
+#pragma unroll
+    for (int k = 0; k < DVP; ++k) o[i][k] = make_float2(0.0f, 0.0f);
+  }
+
+  const int ntile = j1 > j0 ? (j1 - j0 + T - 1) / T : 0;
+  const int tpc = kRowChunk / T;  // tiles per lookup pass
+  if (ntile > 0) {
+    lookup(0);
     __syncthreads();
+    issue(0);
+  }
+  for (int tt = 0; tt < ntile; ++tt) {
+    if (tt + 1 < ntile) {
+      if ((tt + 1) % tpc == 0) {  // rows[] was last read by issue(tt), before the syncs below
+        lookup((tt + 1) / tpc);
+        __syncthreads();
+      }
+      issue(tt + 1);
+    } else {
+      cp_async_commit();  // empty group: wait_group 1 then covers tile tt
+    }
+    cp_async_wait_prev();
+    __syncthreads();
+
+    const int bb = tt & 1;
+    const __nv_bfloat16* kt = ksm + (size_t)bb * T * KS;
+    const __nv_bfloat16* vt = vsm + (size_t)bb * T * Dv;
+    float acc[HPW];
 #pragma unroll
-    for (int i = 0; i < HPW; ++i) {
-      const int h = warp + kAttnWarps * i;
-      if (h < Hq) {
-        float dot = 0.0f;
-        for (int d = lane; d < Dqk; d += 32)
-          dot = fmaf(__bfloat162float(qs[h * Dqk + d]), krow[d], dot);
-        dot = warp_sum(dot);
-        const float z = dot * a.scale_log2;
-        const float mn = fmaxf(m[i], z);
-        const float c = exp2f(m[i] - mn);
-        const float pz = exp2f(z - mn);
-        l[i] = l[i] * c + pz;
+    for (int i = 0; i < HPW; ++i) acc[i] = 0.0f;
+    const bool rv = lane < T && valid[bb * kMaxTile + lane];
+    if (lane < T) {
+      const uint4* kr = reinterpret_cast<const uint4*>(kt + (size_t)lane * KS);
+      for (int c = 0; c < kp8; ++c) {
+        const uint4 kv = kr[c];
 #pragma unroll
-        for (int k = 0; k < DVL; ++k) {
-          const int d = lane + 32 * k;
-          const float v = d < Dv ? vrow[d] : 0.0f;
-          o[i][k] = fmaf(o[i][k], c, pz * v);
+        for (int i = 0; i < HPW; ++i) {
+          const int h = warp + kAttnWarps * i;
+          if (h < Hq)
+            acc[i] = dot8(reinterpret_cast<const uint4*>(qs + (size_t)h * Dqk)[c], kv, acc[i]);
         }
-        m[i] = mn;
       }
     }
-    __syncthreads();
+    float pr[HPW];
+#pragma unroll
+    for (int i = 0; i < HPW; ++i) {
+      pr[i] = 0.0f;
+      const float z = rv ? acc[i] * a.scale_log2 : -INFINITY;
+      const float mt = warp_max(z);
+      if (mt == -INFINITY) continue;  // no valid row in this tile (warp-uniform)
+      const float mn = fmaxf(m[i], mt);
+      const float c = exp2f(m[i] - mn);
+      pr[i] = exp2f(z - mn);
+      l[i] = l[i] * c + pr[i];
+#pragma unroll
+      for (int k = 0; k < DVP; ++k) {
+        o[i][k].x *= c;
+        o[i][k].y *= c;
+      }
+      m[i] = mn;
+    }
+    for (int t = 0; t < T; ++t) {
+      float2 v[DVP];
+#pragma unroll
+      for (int k = 0; k < DVP; ++k) {
+        const int d = 2 * lane + 64 * k;
+        v[k] = d < Dv ? __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162*>(vt + (size_t)t * Dv + d))
+                      : make_float2(0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int i = 0; i < HPW; ++i) {
+        const float pt = __shfl_sync(0xffffffffu, pr[i], t);
+#pragma unroll
+        for (int k = 0; k < DVP; ++k) {
+          o[i][k].x = fmaf(pt, v[k].x, o[i][k].x);
+          o[i][k].y = fmaf(pt, v[k].y, o[i][k].y);
+        }
+      }
+    }
+    __syncthreads();  // buffer bb is refilled by issue(tt + 2)
   }
 
 #pragma unroll
   for (int i = 0; i < HPW; ++i) {
     const int h = warp + kAttnWarps * i;
     if (h >= Hq) continue;
+    const float lt = warp_sum(l[i]);
     if (S == 1) {
-      const float inv = l[i] > 0.0f ? 1.0f / l[i] : 0.0f;
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
       __nv_bfloat16* dst = a.out + ((long long)r * Hq + h) * Dv;
 #pragma unroll
-      for (int k = 0; k < DVL; ++k) {
-        const int d = lane + 32 * k;
-        if (d < Dv) dst[d] = __float2bfloat16(o[i][k] * inv);
+      for (int k = 0; k < DVP; ++k) {
+        const int d = 2 * lane + 64 * k;
+        if (d < Dv) {  // two scalar stores: out need only be 2-byte aligned
+          dst[d] = __float2bfloat16(o[i][k].x * inv);
+          dst[d + 1] = __float2bfloat16(o[i][k].y * inv);
+        }
       }
       if (a.lse && lane == 0)
         a.lse[(long long)r * Hq + h] =
-            l[i] > 0.0f ? (m[i] + log2f(l[i])) * 0.6931471805599453f : -INFINITY;
+            lt > 0.0f ? (m[i] + log2f(lt)) * 0.6931471805599453f : -INFINITY;
     } else {
       float* po = a.part_o + (((long long)r * S + split) * Hq + h) * Dv;
 #pragma unroll
-      for (int k = 0; k < DVL; ++k) {
-        const int d = lane + 32 * k;
-        if (d < Dv) po[d] = o[i][k];
+      for (int k = 0; k < DVP; ++k) {
+        const int d = 2 * lane + 64 * k;
+        if (d < Dv) *reinterpret_cast<float2*>(po + d) = o[i][k];
       }
       if (lane == 0) {
         float* pml = a.part_ml + (((long long)r * S + split) * Hq + h) * 2;
         pml[0] = m[i];
-        pml[1] = l[i];
+        pml[1] = lt;
       }
     }
   }
@@ -148,23 +264,38 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnParams a) {
   grid_dependency_wait();
   launch_dependents();
   const int h = blockIdx.x, r = blockIdx.y, S = a.S, Hq = a.Hq, Dv = a.Dv;
-  __shared__ float wsh[64];
+  __shared__ float wsh[kMaxSplits];
   __shared__ float lsum_sh, mmax_sh;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // S <= 64: lane s holds splits s and s + 32
+    const int lane = threadIdx.x;
+    float ms[2], ls[2];
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) {
-      const float* pml = a.part_ml + (((long long)r * S + s) * Hq + h) * 2;
-      if (pml[1] > 0.0f) M = fmaxf(M, pml[0]);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      ms[u] = -INFINITY;
+      ls[u] = 0.0f;
+      if (s < S) {
+        const float* pml = a.part_ml + (((long long)r * S + s) * Hq + h) * 2;
+        ms[u] = pml[0];
+        ls[u] = pml[1];
+        if (ls[u] > 0.0f) M = fmaxf(M, ms[u]);
+      }
     }
+    M = warp_max(M);
     float lsum = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      const float* pml = a.part_ml + (((long long)r * S + s) * Hq + h) * 2;
-      const float wgt = pml[1] > 0.0f ? exp2f(pml[0] - M) : 0.0f;
-      wsh[s] = wgt;
-      lsum += pml[1] * wgt;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      const float wgt = ls[u] > 0.0f ? exp2f(ms[u] - M) : 0.0f;
+      if (s < S) wsh[s] = wgt;
+      lsum += ls[u] * wgt;
     }
-    lsum_sh = lsum;
-    mmax_sh = M;
+    lsum = warp_sum(lsum);
+    if (lane == 0) {
+      lsum_sh = lsum;
+      mmax_sh = M;
+    }
   }
   __syncthreads();
   const float lsum = lsum_sh;
@@ -180,11 +311,11 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnParams a) {
         lsum > 0.0f ? (mmax_sh + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
 }
 
-constexpr int kMaxSplits = 64;
-
+// Splits of a query's K rows: enough CTAs for two per SM, each at least one
+// full tile of rows.
 int choose_splits(int Nq, int K) {
   int s = (2 * 152 + Nq - 1) / (Nq > 0 ? Nq : 1);
-  int maxs = K / 64;
+  int maxs = K / kMaxTile;
   if (maxs < 1) maxs = 1;
   if (s > maxs) s = maxs;
   if (s > kMaxSplits) s = kMaxSplits;
@@ -192,23 +323,26 @@ int choose_splits(int Nq, int K) {
   return s;
 }
 
-template <int HPW, int DVL>
+template <int HPW, int DVP>
 int launch_generic(const AttnParams& p, cudaStream_t s) {
-  auto kern = k_attn_generic<HPW, DVL>;
-  const size_t smem = (size_t)p.Hq * p.Dqk * 2 + sizeof(float) * (p.Dqk + p.Dv);
-  const int arc = ensure_dynamic_smem((const void*)kern, 200 * 1024, "sparse_attn");
+  auto kern = k_attn_generic<HPW, DVP>;
+  int T = kMaxTile;  // largest tile whose double buffer fits
+  while (T > 1 && generic_smem(p.Hq, p.Dqk, p.Dv, T) > (size_t)kSmemLimit) T >>= 1;
+  const size_t smem = generic_smem(p.Hq, p.Dqk, p.Dv, T);
+  const int arc = ensure_dynamic_smem((const void*)kern, (int)smem, "sparse_attn");
   if (arc) return arc;
-  kern<<<dim3(p.S, p.Nq), kAttnThreads, smem, s>>>(p);
+  kern<<<dim3(p.S, p.Nq), kAttnThreads, smem, s>>>(p, T);
   count_launch();
   return check_launch("sparse_attn");
 }
 
 template <int HPW>
 int launch_dv(const AttnParams& p, cudaStream_t s) {
-  const int dvl = (p.Dv + 31) / 32;
-  if (dvl <= 4) return launch_generic<HPW, 4>(p, s);
-  if (dvl <= 8) return launch_generic<HPW, 8>(p, s);
-  return launch_generic<HPW, 16>(p, s);
+  const int dvp = (p.Dv + 63) / 64;  // bf16 pairs per lane
+  if (dvp <= 1) return launch_generic<HPW, 1>(p, s);
+  if (dvp <= 2) return launch_generic<HPW, 2>(p, s);
+  if (dvp <= 4) return launch_generic<HPW, 4>(p, s);
+  return launch_generic<HPW, 8>(p, s);
 }
 
 }  // namespace

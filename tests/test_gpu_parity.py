@@ -439,3 +439,54 @@ def test_variable_length_prefill_batch():
     lens = (300, 129, 64, 450, 1)
     c = _mixed(620, lens, lens, 64)
     _full_check(c)
+
+
+def _random_selection(rng, Nq, K, hi):
+    """idx [Nq, K]: for query r, distinct positions below hi[r] in random order,
+    with -1 entries scattered among them (padding need not be at the end)."""
+    idx = np.full((Nq, K), -1, np.int32)
+    for r in range(Nq):
+        n = min(int(hi[r]), K - K // 7)
+        row = np.full(K, -1, np.int32)
+        row[:n] = rng.choice(int(hi[r]), size=n, replace=False)
+        idx[r] = rng.permutation(row)
+    return idx
+
+
+@pytest.mark.parametrize("name,kw,K", [
+    # 5 heads (3 warps idle), Dqk 72 (2-way bank conflicts), Dv 8 (4 active lanes)
+    ("odd-dv8", dict(seq_lens=(3000, 700, 1), Hq=5, Dqk=72, Dv=8), 1000),
+    # Dv 200: the last pair block is partly outside Dv; many splits per query
+    ("odd-dv200", dict(seq_lens=(5000, 2500), Hq=9, Dqk=64, Dv=200), 1500),
+    # q of 64 heads x 1536 leaves room for 4-row tiles only
+    ("tile4", dict(seq_lens=(900, 1300), Hq=64, Dqk=1536, Dv=512), 300),
+])
+def test_cuda_core_attention_tiles_and_odd_shapes(name, kw, K):
+    """The CUDA-core attention kernel (shapes the tensor-core kernel does not
+    take): odd head counts and value widths, tiles shorter than 32 rows,
+    selections in random order with -1 entries anywhere."""
+    need_gpu()
+    c = W.make_case(name, seed=1700 + K, K=K, latent=False, H_i=4, D_i=64, idx_dtype="bf16", **kw)
+    g = GpuRun(c)
+    rng = np.random.default_rng(K)
+    idx = _random_selection(rng, c.Nq, c.K, c.seq_lens[c.q_seq])
+    out, lse = g.attn(torch.from_numpy(idx).cuda())
+    out_ref, lse_ref = oracle_attn(c, idx)
+    assert_out_close(out, lse, out_ref, lse_ref, name)
+    assert g.status() == 0
+
+
+def test_cuda_core_attention_long_ranges_per_cta():
+    """Enough queries that each CTA takes all K selected rows of its query:
+    600 rows = three passes of row lookups, 19 tiles (the last one ragged)."""
+    need_gpu()
+    rows = np.sort(np.random.default_rng(3).choice(1200, size=400, replace=False))
+    c = W.make_case("long-range", seed=1750, kind="prefill", T=1200, q_rows=rows, K=600,
+                    **TINY_SHAPES)
+    g = GpuRun(c)
+    rng = np.random.default_rng(4)
+    idx = _random_selection(rng, c.Nq, c.K, c.q_pos + 1)
+    out, lse = g.attn(torch.from_numpy(idx).cuda())
+    out_ref, lse_ref = oracle_attn(c, idx)
+    assert_out_close(out, lse, out_ref, lse_ref, "long-range")
+    assert g.status() == 0
