@@ -222,11 +222,17 @@ def ncu_traffic(kernel_key, src_files):
 
 
 # ---------------------------------------------------------------- workloads --
+PREFILL_TOKENS = None  # --prefill-tokens: a shorter prompt (profiling captures)
+
+
 def workload_case(name, rank):
     import workloads as W
     # weak scaling: every rank draws its own batch
     seeds = {"dec-tiny": 0, "dec-batch": 1, "prefill": 2, "long-dec": 3, "million": 4}
-    return W.config(name, seed=seeds[name] + 1000 * rank)
+    kw = {}
+    if name == "prefill" and PREFILL_TOKENS:
+        kw["T"] = PREFILL_TOKENS
+    return W.config(name, seed=seeds[name] + 1000 * rank, **kw)
 
 
 def algorithmic(case):
@@ -732,8 +738,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=None,
+                    help="prompt length of the prefill workload (default 16384; smaller "
+                         "prompts are for profiler captures, not bench lines)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    global PREFILL_TOKENS
+    PREFILL_TOKENS = args.prefill_tokens
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

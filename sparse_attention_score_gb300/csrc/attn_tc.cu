@@ -82,8 +82,9 @@ struct __align__(1024) Smem {
   uint8_t phi[kPBytes];              // P^T, bf16 part
   uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi), short queries only
   uint64_t kfull[kChunks], kempty[kChunks], qfull[kQRing], qempty[kQRing];
-  uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done;
-  int rowtab[kRows];  // physical rows of the producer's current tile
+  uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done, vfull[2];
+  int rowtab[kRows];     // physical rows of the producer's current tile
+  int valid[2][kRows];   // usable rows of tiles u (slot u % 2), for the softmax
   uint32_t tmem_base;
   int abort;
   int rescale[2];
@@ -304,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.smsync, kSoftmaxThreads);
     mbar_init(&sm.prsync, 128);
     mbar_init(&sm.done, 1);
+    mbar_init(&sm.vfull[0], 128);
+    mbar_init(&sm.vfull[1], 128);
     fence_mbar_init();
   }
   if (threadIdx.x < kHq) {
@@ -340,12 +343,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int u = 0;
     int p_cur = w.ok ? sel_pos(a, w.s, (long long)w.t * kRows + pt) : -1;
     while (w.ok && ok) {
-      const long long row_cur = pos_row(a, w.s, p_cur, false);
+      const long long row_cur = pos_row(a, w.s, p_cur, true);
       Walker nx = w;
       nx.next(a, g);
       const int p_next = nx.ok ? sel_pos(a, nx.s, (long long)nx.t * kRows + pt) : -1;
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
       sm.rowtab[pt] = (int)row_cur;
+      // The softmax of tile u reads valid[u % 2]; the slot is written again
+      // for tile u + 2 only after this producer has passed the slot waits of
+      // tile u + 1, i.e. after PV(u), which follows that softmax.
+      sm.valid[u & 1][pt] = row_cur >= 0 ? 1 : 0;
+      mbar_arrive(&sm.vfull[u & 1]);
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
       for (int i = 0; i < kChunks && ok; ++i) {
         const int c = chunk_at(i);
@@ -489,11 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      // validity of this thread's row is looked up one tile ahead
-      bool valid_next = pos_row(a, s, sel_pos(a, s, (long long)s.t0 * kRows + row), true) >= 0;
       bool pend_l = false;  // reds hold a tile's sums not yet added to l_run
       for (int t = s.t0; t < s.act_end; ++t) {
-        const bool valid = valid_next;
+        // usable rows of the tile, as the producer looked them up
+        if (!warp_wait(&sm.vfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
+        const bool valid = sm.valid[u & 1][row] != 0;
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ta = tbase + lanes + kColS + 64 * (u & 1);
@@ -507,8 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
           sm.redm[quad][32 * half + lane] = butterfly32<true>(v, lane);
         }
-        if (t + 1 < s.act_end)
-          valid_next = pos_row(a, s, sel_pos(a, s, (long long)(t + 1) * kRows + row), true) >= 0;
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
         if (half == 0 && row < kHq) {
           // thread h owns head h: the previous tile's sums, then the new max

@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ql = g * kGroupQ + kQPerWarp * qsel + j;  // query within the block
             const uint32_t taddr = tbase + ((uint32_t)(quad * 32) << 16) + acc * 256 +
                                    (kQPerWarp * qsel + j) * kHeads;
+            // the weights are read four at a time: with one shared-memory load
+            // per FMA the shared-memory pipe paced the epilogue
+            const float4* wq = reinterpret_cast<const float4*>(s.w[ql]);
             uint32_t v[32];
             float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
@@ -302,9 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_32cols(taddr + 32 * hh, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; h += 2) {
-                s0 = fmaf(s.w[ql][32 * hh + h], fmaxf(__uint_as_float(v[h]), 0.0f), s0);
-                s1 = fmaf(s.w[ql][32 * hh + h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+              for (int h = 0; h < 32; h += 4) {
+                const float4 wv = wq[(32 * hh + h) >> 2];
+                s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[h]), 0.0f), s0);
+                s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[h + 1]), 0.0f), s1);
+                s0 = fmaf(wv.z, fmaxf(__uint_as_float(v[h + 2]), 0.0f), s0);
+                s1 = fmaf(wv.w, fmaxf(__uint_as_float(v[h + 3]), 0.0f), s1);
               }
             }
             sc[j] = (s0 + s1) + 0.0f;
