@@ -87,7 +87,7 @@ struct __align__(1024) Smem {
   int valid[2][kRows];   // usable rows of tiles u (slot u % 2), for the softmax
   uint32_t tmem_base;
   int abort;
-  int rescale[2];
+  int rescale[3], slow[3];  // per tile u: slot u % 3
   float redm[4][kHq], reds[4][kHq];
   float m_used[kHq], fscale[kHq], l_run[kHq], l_inv[kHq];
 };
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
-    sm.rescale[0] = sm.rescale[1] = 0;
+    for (int i = 0; i < 3; ++i) sm.rescale[i] = sm.slow[i] = 0;
     for (int i = 0; i < kChunks; ++i) {
       mbar_init(&sm.kfull[i], 128);
       mbar_init(&sm.kempty[i], 1);
@@ -355,6 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm.valid[u & 1][pt] = row_cur >= 0 ? 1 : 0;
       mbar_arrive(&sm.vfull[u & 1]);
       if (!group_sync(&sm.prsync, ps, &sm.abort)) { ok = false; break; }
+      int prows[kRows / 16];
+#pragma unroll
+      for (int k = 0; k < kRows / 16; ++k) prows[k] = sm.rowtab[r0 + 16 * k];
       for (int i = 0; i < kChunks && ok; ++i) {
         const int c = chunk_at(i);
         if (u > 0 && !warp_wait(&sm.kempty[c], (u - 1) & 1, &sm.abort)) { ok = false; break; }
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kRows / 16; ++k) {
           const int r = r0 + 16 * k;
-          const int prow = sm.rowtab[r];
+          const int prow = prows[k];
           const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + c * 128 + gq * 16 : kv;
           cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
         }
@@ -497,7 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      bool pend_l = false;  // reds hold a tile's sums not yet added to l_run
+      // lane l of this warp accumulates, over the warp's 32 rows of every
+      // tile, the softmax denominator of head 32 * half + l
+      float l_acc = 0.0f;
       for (int t = s.t0; t < s.act_end; ++t) {
         // usable rows of the tile, as the producer looked them up
         if (!warp_wait(&sm.vfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
@@ -505,40 +510,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&sm.sfull[u & 1], (u >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ta = tbase + lanes + kColS + 64 * (u & 1);
-        // pass 1: per-head maximum of the tile (this warp's 32 heads)
+        float z[32];  // scores of this row for the warp's 32 heads, log2 units
         {
           uint32_t raw[32];
           tmem_ld_32cols(ta + 32 * half, raw);
           tmem_wait_ld();
-          float v[32];
+          bool exc = false;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
-          sm.redm[quad][32 * half + lane] = butterfly32<true>(v, lane);
-        }
-        if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        if (half == 0 && row < kHq) {
-          // thread h owns head h: the previous tile's sums, then the new max
-          const int h = row;
-          if (pend_l)
-            sm.l_run[h] = sm.l_run[h] * sm.fscale[h] +
-                          ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
-          const float mt = fmaxf(fmaxf(sm.redm[0][h], sm.redm[1][h]),
-                                 fmaxf(sm.redm[2][h], sm.redm[3][h]));
-          const float mo = sm.m_used[h];
-          float mn = mo, f = 1.0f;
-          if (mt > mo + kRescaleLog2 || (mo == -INFINITY && mt > -INFINITY)) {
-            mn = mt;
-            if (mo > -INFINITY) {
-              f = exp2f(mo - mn);
-              sm.rescale[u & 1] = 1;
-            }
+          for (int i = 0; i < 32; ++i) {
+            z[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
+            // a head's running max is raised only when a score exceeds it by
+            // more than 2^8 (the first usable row of a query always does)
+            exc |= z[i] > sm.m_used[32 * half + i] + kRescaleLog2;
           }
-          sm.m_used[h] = mn;
-          sm.fscale[h] = f;
+          if (__any_sync(0xffffffffu, exc) && lane == 0) atomicOr(&sm.slow[u % 3], 1);
+        }
+        // slot (u + 1) % 3 was last read in tile u - 2, before every thread
+        // arrived at tile u - 1's barrier; it is set again in tile u + 1,
+        // after this thread's arrival at tile u's barrier
+        if (half == 0 && row == 0) {
+          sm.slow[(u + 1) % 3] = 0;
+          sm.rescale[(u + 1) % 3] = 0;
         }
         if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
-        const bool resc = sm.rescale[u & 1] != 0;
-        if (half == 0 && row == 0) sm.rescale[(u + 1) & 1] = 0;
+        const bool slow = sm.slow[u % 3] != 0;
+        bool resc = false;
+        if (slow) {
+          // per-head maximum of the tile over all 128 rows, then the new
+          // running maxima and their rescale factors (thread h: head h)
+          // (the butterfly consumes z; it is read again from TMEM below, so
+          // that the rare path holds no second copy of the row in registers)
+          sm.redm[quad][32 * half + lane] = butterfly32<true>(z, lane);
+          if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
+          if (half == 0 && row < kHq) {
+            const int h = row;
+            const float mt = fmaxf(fmaxf(sm.redm[0][h], sm.redm[1][h]),
+                                   fmaxf(sm.redm[2][h], sm.redm[3][h]));
+            const float mo = sm.m_used[h];
+            float mn = mo, f = 1.0f;
+            if (mt > mo + kRescaleLog2 || (mo == -INFINITY && mt > -INFINITY)) {
+              mn = mt;
+              if (mo > -INFINITY) {
+                f = exp2f(mo - mn);
+                sm.rescale[u % 3] = 1;
+              }
+            }
+            sm.m_used[h] = mn;
+            sm.fscale[h] = f;
+          }
+          if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }
+          resc = sm.rescale[u % 3] != 0;
+          l_acc *= sm.fscale[32 * half + lane];
+          uint32_t raw[32];
+          tmem_ld_32cols(ta + 32 * half, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = valid ? __uint_as_float(raw[i]) * c : -INFINITY;
+        }
         // the previous PV must be done before P^T (and, if needed, O) change
         if (!warp_wait(&sm.pempty, (u & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
@@ -556,15 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // pass 2: P = 2^(z - m) in bf16 (hi + lo for short queries) into this
-        // row of P^T; the per-head sums add the fp32 values
+        // P = 2^(z - m) in bf16 (hi + lo for short queries) into this row of
+        // P^T; the denominators add the fp32 values
         const bool split = s.n <= kSplitRows;
         uint8_t* rh = sm.phi + row * 128;
         uint8_t* rl = sm.plo + row * 128;
         {
-          uint32_t raw[32];
-          tmem_ld_32cols(ta + 32 * half, raw);
-          tmem_wait_ld();
           float v[32];
           uint32_t hw[16], lw[16];
 #pragma unroll
@@ -572,8 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // branch-free: an unusable row gives 2^-inf = 0 (a usable row makes
             // every head's running max finite)
             const float m0 = sm.m_used[32 * half + i], m1 = sm.m_used[32 * half + i + 1];
-            const float p0 = ex2_approx(valid ? __uint_as_float(raw[i]) * c - m0 : -INFINITY);
-            const float p1 = ex2_approx(valid ? __uint_as_float(raw[i + 1]) * c - m1 : -INFINITY);
+            const float p0 = ex2_approx(valid ? z[i] - m0 : -INFINITY);
+            const float p1 = ex2_approx(valid ? z[i + 1] - m1 : -INFINITY);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
             const float2 hf = __bfloat1622float2(hi);
             const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
@@ -591,22 +616,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(rl + off) =
                   make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
           }
-          sm.reds[quad][32 * half + lane] = butterfly32<false>(v, lane);
+          l_acc += butterfly32<false>(v, lane);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.sempty[u & 1]);
         mbar_arrive(&sm.pfull);
-        pend_l = true;
         ++u;
       }
       if (!ok) break;
       // ---- finalize the query segment: O out of TMEM ----
-      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // last tile's sums
+      sm.reds[quad][32 * half + lane] = l_acc;
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // all partial sums
       if (half == 0 && row < kHq) {
         const int h = row;
-        const float l = sm.l_run[h] * sm.fscale[h] +
-                        ((sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]));
+        const float l = (sm.reds[0][h] + sm.reds[1][h]) + (sm.reds[2][h] + sm.reds[3][h]);
         sm.l_run[h] = l;
         sm.l_inv[h] = l > 0.0f ? 1.0f / l : 0.0f;
       }
@@ -641,15 +665,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           pml[2 * row] = m;
           pml[2 * row + 1] = l;
         }
-      }
-      tc_fence_before();
-      mbar_arrive(&sm.ofree);
-      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // stats read
-      if (half == 0 && row < kHq) {
+        // head h's statistics are read by thread h only; reset them before
+        // the barrier after which the next query's first tile reads m_used
         sm.m_used[row] = -INFINITY;
         sm.l_run[row] = 0.0f;
         sm.fscale[row] = 1.0f;
       }
+      tc_fence_before();
+      mbar_arrive(&sm.ofree);
+      if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // stats read, reset
       ++sa;
       ok = ok && !sm.abort;
     }
