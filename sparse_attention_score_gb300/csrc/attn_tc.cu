@@ -23,8 +23,9 @@
 // each weight of the output's average of V rows is within 2^-9 (relative) of
 // its exact value and lse keeps fp32 accuracy.  A query with fewer rows has a
 // peaked softmax and an output close to a few single V rows, so there P is
-// kept as bf16 hi + lo (two PV MMAs) and the output is exact up to its final
-// bf16 store.
+// kept as bf16 hi + lo (two PV passes, the remainder written over the bf16
+// part once the first pass has read it) and the output is exact up to its
+// final bf16 store.
 // The tiles of all queries are laid end to end and split evenly over one CTA
 // per SM.  A query whose tiles span several CTAs leaves one unnormalised
 // partial (O, m, l) per CTA in the workspace and a second small kernel merges
@@ -38,10 +39,11 @@
 //   into the 128-byte swizzled layout, 8 consecutive threads per 128-byte
 //   row chunk (rows of 1152 bytes anywhere in the pool); the tile stays
 //   resident from QK to PV, each chunk slot refilled for the next tile as
-//   soon as its last MMA is done (chunk 8 right after QK, chunks 0-7 after
-//   their PV block);
-//   warp 8 TMEM owner and MMA issuer; warp 9 streams Q's chunks from L2 by
-//   TMA through a five-slot ring.
+//   soon as its last MMA is done (chunks 0-7 after their PV block, chunk 8,
+//   needed by QK only and taken last, after the PV: from the softmax to the
+//   PV its slot holds P^T);
+//   warp 8 TMEM owner and MMA issuer; warp 9 loads the query's Q (72 KB) by
+//   TMA once per query, resident while the CTA works on that query.
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
@@ -59,9 +61,8 @@ constexpr int kHq = 64, kDqk = 576, kDv = 512;
 constexpr int kRows = 128;
 constexpr int kChunks = kDqk / 64;           // 9 K chunks of 64 dims; the first 8 are V
 constexpr int kChunkBytes = kRows * 128;     // 64 dims x 128 rows, bf16
-constexpr int kQRing = 5;                    // Q chunks in flight
+constexpr int kCopyLag = 2;                  // producer: copy groups in flight before an arrival
 constexpr int kQChunkBytes = kHq * 128;      // 8 KB
-constexpr int kPBytes = kRows * 128;         // P^T: 64 heads (128 B) per row
 constexpr int kThreads = 448;         // softmax 0-3 + 10-13, producer 4-7, MMA 8, Q loader 9
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -72,16 +73,14 @@ constexpr long long kSplitRows = 512;  // queries with at most this many rows: P
 constexpr int kMaxCtas = 160;
 constexpr uint32_t kIdescQK = instr_desc(128, kHq, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
-// Chunk order within a tile: chunk 8 (needed by QK only) first, because its
-// slot is the first one the previous tile releases.
-__device__ __forceinline__ int chunk_at(int i) { return i == 0 ? 8 : i - 1; }
+constexpr int kPSlot = kChunks - 1;  // chunk 8 (QK only): its slot holds P^T from softmax to PV
 
 struct __align__(1024) Smem {
-  uint8_t kv[kChunks][kChunkBytes];  // the tile's rows, resident from QK to PV
-  uint8_t q[kQRing][kQChunkBytes];   // Q chunks streamed from L2
-  uint8_t phi[kPBytes];              // P^T, bf16 part
-  uint8_t plo[kPBytes];              // P^T, bf16 remainder (P - phi), short queries only
-  uint64_t kfull[kChunks], kempty[kChunks], qfull[kQRing], qempty[kQRing];
+  // the tile's rows, chunks 0-7 resident from QK to PV; once QK is done,
+  // chunk 8's slot holds P^T (one 128-byte row of 64 bf16 heads per row)
+  uint8_t kv[kChunks][kChunkBytes];
+  uint8_t q[kChunks][kQChunkBytes];  // the current query's Q, loaded once per query
+  uint64_t kfull[kChunks], kempty[kChunks], qfull, qempty, phidone, plofull;
   uint64_t sfull[2], sempty[2], pfull, pempty, ofull, ofree, smsync, prsync, done, vfull[2];
   int rowtab[kRows];     // physical rows of the producer's current tile
   int valid[2][kRows];   // usable rows of tiles u (slot u % 2), for the softmax
@@ -91,6 +90,8 @@ struct __align__(1024) Smem {
   float redm[4][kHq], reds[4][kHq];
   float m_used[kHq], fscale[kHq], l_run[kHq], l_inv[kHq];
 };
+
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of k_attn_tc");
 
 struct Geo {
   int Tq;     // tiles per query (uniform item grid)
@@ -253,13 +254,8 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                "r"(src_bytes)
                : "memory");
 }
-// One arrival on `bar` once every cp.async this thread has issued so far has
-// landed; the thread does not wait (the arrival counts toward the barrier's
-// expected count).  The consumer makes the data visible to the tensor cores
-// with a proxy fence after its wait.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -290,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.kfull[i], 128);
       mbar_init(&sm.kempty[i], 1);
     }
-    for (int i = 0; i < kQRing; ++i) {
-      mbar_init(&sm.qfull[i], 1);
-      mbar_init(&sm.qempty[i], 1);
-    }
+    mbar_init(&sm.qfull, 1);
+    mbar_init(&sm.qempty, 1);
+    mbar_init(&sm.phidone, 1);
+    mbar_init(&sm.plofull, kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.sfull[i], 1);
       mbar_init(&sm.sempty[i], kSoftmaxThreads);
@@ -330,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each 128-byte row chunk is copied by 8 consecutive threads (16 B each),
     // so a warp instruction moves four whole rows; thread t copies granule
     // t % 8 of rows t / 8 + 16 i.  The tile's physical rows are looked up
-    // once (thread t: row t) into a shared table.  A chunk's full barrier
-    // is armed by the copies themselves, so the producer never waits for
-    // its own loads: every slot is refilled as soon as it is released.
+    // once (thread t: row t) into a shared table, and each thread keeps its
+    // eight rows in registers for the tile's nine chunks (a shared-memory
+    // load issued behind pending copies waits for them).  Every slot is
+    // refilled as soon as it is released.  Completion is tracked by copy
+    // groups: cp.async.mbarrier.arrive.noinc arrivals were measured to cap
+    // one SM's copies at about a third of the rate of groups.
     const int pt = threadIdx.x - 128;
     const int gq = pt & 7, r0 = pt >> 3;
     const char* kv = reinterpret_cast<const char*>(a.kp);
@@ -358,8 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int prows[kRows / 16];
 #pragma unroll
       for (int k = 0; k < kRows / 16; ++k) prows[k] = sm.rowtab[r0 + 16 * k];
+      // One copy group per chunk; chunk i's full barrier gets one plain
+      // arrival per thread once its group has landed, checked when chunk
+      // i + 2 has been issued (and for the last two at the end of the tile).
+      // Every slot wait of this tile depends only on the previous tile's
+      // chunks, all of which have been arrived, so the lag cannot deadlock.
+#pragma unroll 1
       for (int i = 0; i < kChunks && ok; ++i) {
-        const int c = chunk_at(i);
+        const int c = i;
         if (u > 0 && !warp_wait(&sm.kempty[c], (u - 1) & 1, &sm.abort)) { ok = false; break; }
         uint8_t* base = sm.kv[c];
 #pragma unroll
@@ -369,8 +374,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const char* src = prow >= 0 ? kv + (size_t)prow * (kDqk * 2) + c * 128 + gq * 16 : kv;
           cp_async16(base + r * 128 + ((gq ^ (r & 7)) << 4), src, prow >= 0 ? 16u : 0u);
         }
-        cp_async_arrive(&sm.kfull[c]);
+        cp_async_commit();
+        if (i >= kCopyLag) {
+          cp_async_wait<kCopyLag>();
+          mbar_arrive(&sm.kfull[i - kCopyLag]);
+        }
       }
+      if (!ok) break;
+      cp_async_wait<0>();
+#pragma unroll
+      for (int i = kChunks - kCopyLag; i < kChunks; ++i) mbar_arrive(&sm.kfull[i]);
       p_cur = p_next;
       w = nx;
       ++u;
@@ -382,17 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       Walker w;
       w.init(a, g, r_first, r_last);
-      int qs = 0;
+      int nq = 0, cur = -1;
       bool ok = true;
       while (w.ok && ok) {
-        for (int i = 0; i < kChunks; ++i, ++qs) {
-          const int slot = qs % kQRing;
-          if (qs >= kQRing && !mbar_wait(&sm.qempty[slot], ((qs / kQRing) - 1) & 1, &sm.abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.qfull[slot], kQChunkBytes);
-          tma_load_2d(sm.q[slot], &map_q, &sm.qfull[slot], 64 * chunk_at(i), w.r * kHq);
+        if (w.r != cur) {  // a new query: its Q replaces the previous one's after its last QK
+          cur = w.r;
+          if (nq > 0 && !mbar_wait(&sm.qempty, (nq - 1) & 1, &sm.abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.qfull, kChunks * kQChunkBytes);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(sm.q[c], &map_q, &sm.qfull, 64 * c, w.r * kHq);
+          ++nq;
         }
         w.next(a, g);
       }
@@ -401,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      int u = 0, sa = 0, qs = 0, cur_r = -1;
+      int u = 0, sa = 0, ns = 0, cur_r = -1;  // ns: tiles with P as hi + lo so far
       bool ok = true;
       Walker w;
       w.init(a, g, r_first, r_last);
@@ -410,58 +422,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.r != cur_r) {
           cur_r = w.r;
           ++sa;
+          if (!mbar_wait(&sm.qfull, (sa - 1) & 1, &sm.abort)) { ok = false; break; }
         }
         if (!mbar_wait(&sm.sempty[u & 1], ((u >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dS = tbase + kColS + 64 * (u & 1);
-        for (int i = 0; i < kChunks; ++i, ++qs) {
-          const int c = chunk_at(i), slot = qs % kQRing;
-          if (!mbar_wait(&sm.qfull[slot], (qs / kQRing) & 1, &sm.abort) ||
-              !mbar_wait(&sm.kfull[c], u & 1, &sm.abort)) {
+        for (int c = 0; c < kChunks; ++c) {
+          if (!mbar_wait(&sm.kfull[c], u & 1, &sm.abort)) {
             ok = false;
             break;
           }
           fence_proxy_async_smem();  // the copies' writes, seen by the tensor cores
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sm.kv[c]), b0 = smem_u32(sm.q[slot]);
+          const uint32_t a0 = smem_u32(sm.kv[c]), b0 = smem_u32(sm.q[c]);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_f16(dS, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B),
                     smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B), kIdescQK,
-                    (i + k) > 0 ? 1u : 0u);
-          mma_commit(&sm.qempty[slot]);
-          if (c == kChunks - 1) mma_commit(&sm.kempty[c]);  // QK only
+                    (c + k) > 0 ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(&sm.sfull[u & 1]);
-        // PV of this tile once the softmax has written P^T
+        if (last) mma_commit(&sm.qempty);  // this query's Q is read for the last time
+        // PV of this tile once the softmax has written P^T (into chunk 8's slot)
         if (!mbar_wait(&sm.pfull, u & 1, &sm.abort)) { ok = false; break; }
         if (first && sa > 1 && !mbar_wait(&sm.ofree, (sa - 2) & 1, &sm.abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t ph = smem_u32(sm.phi), pl = smem_u32(sm.plo);
+        const uint32_t pt = smem_u32(sm.kv[kPSlot]);
         const bool split = w.s.n <= kSplitRows;
-        for (int blk = 0; blk < kDv / 128; ++blk) {
-          const uint32_t v0 = smem_u32(sm.kv[2 * blk]);  // chunks 2blk, 2blk+1 are 16 KB apart
-          const uint32_t d = tbase + kColO + 64 * blk;
-          if (split) {
+        // split: the bf16 part first, then (once the softmax has written it
+        // over the first) the remainder, releasing the V chunks
+        for (int pass = split ? 0 : 1; pass < 2 && ok; ++pass) {
+          if (pass == 1 && split) {
+            mma_commit(&sm.phidone);
+            if (!mbar_wait(&sm.plofull, ns & 1, &sm.abort)) { ok = false; break; }
+            tc_fence_after();
+            ++ns;
+          }
+          for (int blk = 0; blk < kDv / 128; ++blk) {
+            const uint32_t v0 = smem_u32(sm.kv[2 * blk]);  // chunks 2blk, 2blk+1 are 16 KB apart
+            const uint32_t d = tbase + kColO + 64 * blk;
 #pragma unroll
-            for (int k = 0; k < kRows / 16; ++k) {
-              const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
-              mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
-                      (first && k == 0) ? 0u : 1u);
-              mma_f16(d, va, smem_desc(pl + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV, 1u);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < kRows / 16; ++k) {
-              const uint64_t va = smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B);
-              mma_f16(d, va, smem_desc(ph + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
-                      (first && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kRows / 16; ++k)
+              mma_f16(d, smem_desc(v0 + 2048 * k, kChunkBytes, 1024, kSwizzle128B),
+                      smem_desc(pt + 2048 * k, 8192, 1024, kSwizzle128B), kIdescPV,
+                      (first && k == 0 && pass == (split ? 0 : 1)) ? 0u : 1u);
+            if (pass == 1) {
+              mma_commit(&sm.kempty[2 * blk]);
+              mma_commit(&sm.kempty[2 * blk + 1]);
             }
           }
-          mma_commit(&sm.kempty[2 * blk]);
-          mma_commit(&sm.kempty[2 * blk + 1]);
         }
+        if (!ok) break;
+        mma_commit(&sm.kempty[kPSlot]);  // P^T read: chunk 8's slot may take the next tile
         mma_commit(&sm.pempty);
         if (last) mma_commit(&sm.ofull);
         ++u;
@@ -481,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     const uint32_t lanes = (uint32_t)(quad * 32) << 16;
     const float c = a.scale_log2;
-    int u = 0, sa = 0;
+    int u = 0, sa = 0, ns = 0;  // ns: tiles with P as hi + lo so far
     uint32_t sp = 0;
     bool ok = true;
     for (int r = r_first; r <= r_last && ok; ++r) {
@@ -587,11 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(z - m) in bf16 (hi + lo for short queries) into this row of
         // P^T; the denominators add the fp32 values
         const bool split = s.n <= kSplitRows;
-        uint8_t* rh = sm.phi + row * 128;
-        uint8_t* rl = sm.plo + row * 128;
+        uint8_t* rp = sm.kv[kPSlot] + row * 128;  // QK is done with chunk 8 (sfull)
+        uint32_t lw[16];
         {
           float v[32];
-          uint32_t hw[16], lw[16];
+          uint32_t hw[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             // branch-free: an unusable row gives 2^-inf = 0 (a usable row makes
@@ -610,11 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int off = ((4 * half + k) ^ (row & 7)) << 4;
-            *reinterpret_cast<uint4*>(rh + off) =
+            *reinterpret_cast<uint4*>(rp + off) =
                 make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-            if (split)
-              *reinterpret_cast<uint4*>(rl + off) =
-                  make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
           }
           l_acc += butterfly32<false>(v, lane);
         }
@@ -622,6 +632,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.sempty[u & 1]);
         mbar_arrive(&sm.pfull);
+        if (split) {
+          // the remainder, over the bf16 part once the PV has read that
+          if (!warp_wait(&sm.phidone, ns & 1, &sm.abort)) { ok = false; break; }
+          ++ns;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int off = ((4 * half + k) ^ (row & 7)) << 4;
+            *reinterpret_cast<uint4*>(rp + off) =
+                make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&sm.plofull);
+        }
         ++u;
       }
       if (!ok) break;
