@@ -362,6 +362,9 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
         stage[:, k] = [a_.elapsed_time(b_) for a_, b_ in sev]
     status = pipe.status()
     cache_write = measure_cache_write(dsa, case, d, layout, dev, flush, steps)
+    step_calls = None
+    if kind == "prefill":
+        step_calls = measure_prefill_steps(dsa, case, d, layout, dev, flush, steps)
 
     e2e = None
     if do_e2e:
@@ -370,7 +373,7 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     total_ms = max_over_ranks(total_ms, world, dev)
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
                 launches=int(launches), launches_per=launches_per, clocks=clocks, status=status,
-                e2e=e2e, graph=graphs["step"], cache_write=cache_write)
+                e2e=e2e, graph=graphs["step"], cache_write=cache_write, step_calls=step_calls)
 
 
 def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
@@ -415,6 +418,64 @@ def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
     return {"rows": n, "bytes_per_row": int(row_bytes), "us": round(us, 2),
             "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "status": dsa.get_status(ws)}
+
+
+def measure_prefill_steps(dsa, case, d, layout, dev, flush, steps):
+    """The whole prefill step through one binding call, two ways: the staged
+    dsa_prefill_step (the caller's [Nq][ld] score matrix between the indexer
+    and top-K) and dsa_prefill_step_chunked (one chunk of scores at a time in
+    an L2-sized workspace scratch).  Both include the cache write of the
+    prompt's rows (the rows already cached, read back through the block
+    table, so the cache is unchanged); the index sets must agree."""
+    import torch
+    pl = d.q_pos.long()
+    phys = d.block_table.long()[0, pl // case.bs] * case.bs + pl % case.bs
+    kv_rows = d.k_pool.view(-1, d.k_pool.shape[-1])[phys].contiguous()
+    ki_rows = d.kidx_pool.view(-1, d.kidx_pool.shape[-1])[phys].contiguous()
+    Nq, ld, K = case.Nq, int(case.n_elig.max()), case.K
+    ld = (ld + 3) // 4 * 4
+    scores = torch.empty((Nq, ld), dtype=torch.float32, device=dev)
+    outs = {m: (torch.empty((Nq, K), dtype=torch.int32, device=dev),
+                torch.empty((Nq, case.Hq, case.Dv), dtype=torch.bfloat16, device=dev),
+                torch.empty((Nq, case.Hq), dtype=torch.float32, device=dev))
+            for m in ("staged", "chunked")}
+    ws_s = dsa.workspace(dsa.prefill_step_workspace_size(Nq, case.H_i, case.D_i, ld, case.Hq,
+                                                         case.Dqk, case.Dv, K), device=dev)
+    ws_c = dsa.workspace(dsa.prefill_step_chunked_workspace_size(
+        Nq, case.H_i, case.D_i, ld, case.Hq, case.Dqk, case.Dv, K, 0), device=dev)
+    common = (layout, 0, d.q_pos, d.n_elig, kv_rows, d.k_pool, ki_rows, d.kidx_pool, d.q_idx,
+              d.w, d.q, K, case.sm_scale)
+
+    def staged():
+        i, o, l_ = outs["staged"]
+        dsa.prefill_step(*common, scores, i, o, l_, ws_s)
+
+    def chunked():
+        i, o, l_ = outs["chunked"]
+        dsa.prefill_step_chunked(*common, ld, i, o, l_, ws_c)
+
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name_, fn in (("staged", staged), ("chunked", chunked)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            flush(float(i))
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        res[name_ + "_ms"] = round(float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev])), 4)
+    res["score_bytes_staged"] = int(Nq * ld * 4)
+    res["workspace_bytes_chunked"] = int(ws_c.numel())
+    res["idx_equal"] = bool(torch.equal(outs["staged"][0], outs["chunked"][0]))
+    res["status"] = dsa.get_status(ws_s) | dsa.get_status(ws_c)
+    res["api"] = "dsa_prefill_step vs dsa_prefill_step_chunked, one call each, cache write included"
+    del scores
+    return res
 
 
 def _e2e_inputs(case, dev):
@@ -689,6 +750,8 @@ def headline(args, world, res, peaks):
         "device_status": res["status"],
         "cache_write": res["cache_write"],
     }
+    if res.get("step_calls") is not None:
+        line["step_calls"] = res["step_calls"]
     line["path_roofline"] = path_roofline(case, ms_step, peaks)
     return line
 
@@ -722,7 +785,7 @@ def secondary_line(r2, st2, world, peaks):
             "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
             "gpu_launches": r2["launches"], "gpu_launches_per_step": r2["launches_per"],
             "clocks": r2["clocks"], "device_status": r2["status"],
-            "cache_write": r2["cache_write"]}
+            "cache_write": r2["cache_write"], "step_calls": r2.get("step_calls")}
 
 
 def main():

@@ -332,6 +332,36 @@ int dsa_prefill_step(const dsa_paged_layout* layout, int seq, const int32_t* q_p
                      int K, float sm_scale, float* scores, int64_t ld, int32_t* idx, void* out,
                      float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream);
 
+/* dsa_prefill_step_chunked — "Day-0 Adaptation of Trillion-Parameter MoE Models
+ * on Domestic GPUs", section 3 (3): the prefill stage fuses index selection and
+ * exact attention into large-granularity operators.  The same work as
+ * dsa_prefill_step (cache write, indexer score, top-K, attention; same
+ * arguments and results), without the [Nq][ld] score matrix: the queries are
+ * scored and selected `chunk` rows at a time, and a chunk's scores live in one
+ * scratch region of the workspace that the next chunk overwrites.  The score
+ * memory is chunk x ld x 4 bytes instead of Nq x ld x 4 (a 16384-token prompt:
+ * 48 MB instead of 1 GB), and with the default chunk it stays in L2 between the
+ * indexer that writes it and the top-K that reads it, so the scores make no
+ * round trip through HBM.
+ *  ld          row length of the scratch (>= the largest n_eligible)
+ *  chunk       queries per chunk; 0: the largest multiple of 16 whose scores
+ *              fit 48 MB (at least 16)
+ *  idx, out, lse, ws: as for dsa_prefill_step; ws =
+ *              dsa_prefill_step_chunked_workspace_size(...) bytes, for the same
+ *              chunk argument
+ * Errors: those of dsa_prefill_step; chunk < 0 is DSA_ERR_INVALID.
+ */
+size_t dsa_prefill_step_chunked_workspace_size(int Nq, int H_i, int D_i, int64_t ld, int Hq,
+                                               int Dqk, int Dv, int K, int chunk);
+int dsa_prefill_step_chunked(const dsa_paged_layout* layout, int seq, const int32_t* q_pos,
+                             const int32_t* n_eligible, int Nq, const void* k_new, void* k_pool,
+                             int64_t k_row_stride, const void* v_new, void* v_pool,
+                             int64_t v_row_stride, const void* kidx_new, void* kidx_pool,
+                             int idx_dtype, const void* q_idx, const float* w, int H_i, int D_i,
+                             const void* q, int Hq, int Dqk, int Dv, int K, float sm_scale,
+                             int64_t ld, int chunk, int32_t* idx, void* out, float* lse, void* ws,
+                             size_t ws_bytes, dsa_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Utilities (no counterpart on the pages).
  * dsa_get_status: copy the status word of a workspace to *status (host), after

@@ -94,6 +94,10 @@ _sig("dsa_prefill_step_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, _i, _i])
 _sig("dsa_prefill_step", _i, [_LP, _i, _vp, _vp, _i, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i,
                               _vp, _vp, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _i64, _vp, _vp, _vp,
                               _vp, _sz, _vp])
+_sig("dsa_prefill_step_chunked_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, _i, _i, _i])
+_sig("dsa_prefill_step_chunked", _i, [_LP, _i, _vp, _vp, _i, _vp, _vp, _i64, _vp, _vp, _i64, _vp,
+                                      _vp, _i, _vp, _vp, _i, _i, _vp, _i, _i, _i, _i, _f, _i64, _i,
+                                      _vp, _vp, _vp, _vp, _sz, _vp])
 _sig("dsa_cache_write_workspace_size", _sz, [])
 _sig("dsa_cache_write", _i, [_LP, _vp, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
@@ -113,7 +117,8 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_sparse_attn_prefill_workspace_size", "dsa_sparse_attn_prefill",
            "dsa_cache_write_workspace_size", "dsa_cache_write",
            "dsa_decode_step_workspace_size", "dsa_decode_step",
-           "dsa_prefill_step_workspace_size", "dsa_prefill_step")
+           "dsa_prefill_step_workspace_size", "dsa_prefill_step",
+           "dsa_prefill_step_chunked_workspace_size", "dsa_prefill_step_chunked")
 
 
 def lib() -> ctypes.CDLL:
@@ -417,6 +422,38 @@ def prefill_step(layout: PagedLayout, seq, q_pos, n_eligible, k_new, k_pool, kid
                                K, float(sm_scale), ps, ld, pi, po, pl, pws, ws.numel(),
                                _stream(stream))
     _check(rc, "dsa_prefill_step")
+
+
+def prefill_step_chunked_workspace_size(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K, chunk=0) -> int:
+    return int(_lib.dsa_prefill_step_chunked_workspace_size(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K,
+                                                            int(chunk)))
+
+
+def prefill_step_chunked(layout: PagedLayout, seq, q_pos, n_eligible, k_new, k_pool, kidx_new,
+                         kidx_pool, q_idx, w, q, K, sm_scale, ld, idx, out, lse, ws, chunk=0,
+                         v_new=None, v_pool=None, stream=None):
+    """dsa_prefill_step without the score matrix (include/dsa.h,
+    dsa_prefill_step_chunked): queries scored and selected `chunk` at a time
+    (0: automatic) through a scratch in the workspace."""
+    Nq, Hq, Dqk = q.shape
+    a = _Args(layout).add(q_pos, "q_pos", _I32, Nq).add(n_eligible, "n_eligible", _I32, Nq)
+    H_i, D_i = q_idx.shape[1], q_idx.shape[2]
+    Dv, K, ld = out.shape[2], int(K), int(ld)
+    vp = k_pool if v_pool is None else v_pool
+    ks, vs = k_pool.shape[-1], vp.shape[-1]
+    ke = (q_idx.element_size(),)
+    a.add(k_new, "k_new", _BF16, Nq * Dqk).add(k_pool, "k_pool", _BF16, _rows(layout, ks))
+    a.add(v_new, "v_new", _BF16, Nq * Dv).add(vp, "v_pool", _BF16, _rows(layout, vs))
+    a.add(kidx_new, "kidx_new", ke, Nq * D_i).add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i))
+    a.add(q_idx, "q_idx", _KEY).add(w, "w", _F32, Nq * H_i).add(q, "q", _BF16)
+    a.add(idx, "idx", _I32, Nq * K).add(out, "out", _BF16, Nq * Hq * Dv)
+    a.add(lse, "lse", _F32, Nq * Hq).add(ws, "ws", _WS)
+    (ppos, pn, pkn, pkp, pvn, pvp, pin, pip, pqi, pw, pq, pi, po, pl, pws) = a.ptrs()
+    rc = _lib.dsa_prefill_step_chunked(layout.c(), int(seq), ppos, pn, Nq, pkn, pkp, ks, pvn, pvp,
+                                       vs, pin, pip, _elt_dtype(kidx_pool), pqi, pw, H_i, D_i, pq,
+                                       Hq, Dqk, Dv, K, float(sm_scale), ld, int(chunk), pi, po, pl,
+                                       pws, ws.numel(), _stream(stream))
+    _check(rc, "dsa_prefill_step_chunked")
 
 
 def get_status(ws, clear: bool = True, stream=None) -> int:

@@ -387,4 +387,88 @@ int dsa_prefill_step(const dsa_paged_layout* layout, int seq, const int32_t* q_p
                      L.total - L.off_attn, stream, false, status, seq);
 }
 
+// ---------------------------------------------------------- chunked step --
+// The prefill step without the score matrix: queries are scored and selected
+// a chunk at a time; a chunk's scores go to one scratch region of the
+// workspace, sized for one chunk, which the next chunk overwrites.  With the
+// default chunk the scratch (<= kChunkScoreBytes) stays in L2 between the
+// indexer that writes it and the top-K that reads it.
+constexpr size_t kChunkScoreBytes = 48ull << 20;
+
+static int prefill_chunk_rows(int Nq, int64_t ld, int chunk) {
+  long long c = chunk > 0 ? chunk : (long long)(kChunkScoreBytes / ((size_t)(ld > 0 ? ld : 1) * 4));
+  if (chunk <= 0) c = c / 16 * 16;  // whole blocks of the prefill indexer
+  if (c < 16) c = 16;
+  if (c > Nq) c = Nq;
+  if (c < 1) c = 1;
+  return (int)c;
+}
+
+struct ChunkLayout {
+  size_t off_index, off_topk, off_attn, off_scores, total;
+  int C;
+};
+
+static ChunkLayout chunk_layout(int Nq, int H_i, int D_i, int64_t ld, int Hq, int Dqk, int Dv,
+                                int K, int chunk) {
+  ChunkLayout L;
+  L.C = prefill_chunk_rows(Nq, ld, chunk);
+  L.off_index = kWsHeader;
+  L.off_topk = L.off_index + round256(index_score_ws(L.C, H_i, D_i, (long long)ld));
+  L.off_attn = L.off_topk + round256(topk_ws(L.C, (long long)ld, K));
+  L.off_scores = L.off_attn + round256(attn_ws(Nq, Hq, Dqk, Dv, K, false));
+  L.total = L.off_scores + round256((size_t)L.C * (size_t)ld * sizeof(float));
+  return L;
+}
+
+size_t dsa_prefill_step_chunked_workspace_size(int Nq, int H_i, int D_i, int64_t ld, int Hq,
+                                               int Dqk, int Dv, int K, int chunk) {
+  if (Nq < 1 || ld < 1) return kWsHeader;
+  return chunk_layout(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K, chunk).total;
+}
+
+int dsa_prefill_step_chunked(const dsa_paged_layout* layout, int seq, const int32_t* q_pos,
+                             const int32_t* n_eligible, int Nq, const void* k_new, void* k_pool,
+                             int64_t k_row_stride, const void* v_new, void* v_pool,
+                             int64_t v_row_stride, const void* kidx_new, void* kidx_pool,
+                             int idx_dtype, const void* q_idx, const float* w, int H_i, int D_i,
+                             const void* q, int Hq, int Dqk, int Dv, int K, float sm_scale,
+                             int64_t ld, int chunk, int32_t* idx, void* out, float* lse, void* ws,
+                             size_t ws_bytes, dsa_stream_t stream) {
+  if (!layout) return set_error(DSA_ERR_INVALID, "prefill_step_chunked: NULL layout");
+  if (seq < 0 || seq >= layout->batch)
+    return set_error(DSA_ERR_INVALID, "prefill_step_chunked: seq out of range");
+  if (!q_pos || !n_eligible || !q_idx || !w || !idx)
+    return set_error(DSA_ERR_INVALID, "prefill_step_chunked: NULL pointer");
+  if (Nq < 0 || ld < 1 || chunk < 0)
+    return set_error(DSA_ERR_INVALID, "prefill_step_chunked: need Nq >= 0, ld >= 1, chunk >= 0");
+  if (idx_dtype != DSA_BF16 && idx_dtype != DSA_FP8_E4M3)
+    return set_error(DSA_ERR_UNSUPPORTED, "prefill_step_chunked: idx_dtype BF16 or FP8_E4M3");
+  if (Nq == 0) return DSA_OK;
+  const ChunkLayout L = chunk_layout(Nq, H_i, D_i, ld, Hq, Dqk, Dv, K, chunk);
+  int rc = check_ws(ws, ws_bytes, L.total);
+  if (rc) return rc;
+  char* base = reinterpret_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(ws);
+  float* scratch = reinterpret_cast<float*>(base + L.off_scores);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = step_cache_write(layout, seq, q_pos, Nq, k_new, k_pool, k_row_stride, Dqk, v_new, v_pool,
+                        v_row_stride, Dv, kidx_new, kidx_pool, idx_dtype, D_i, status, s);
+  if (rc) return rc;
+  const size_t qrow = (size_t)H_i * D_i * (idx_dtype == DSA_FP8_E4M3 ? 1 : 2);
+  for (int r0 = 0; r0 < Nq; r0 += L.C) {
+    const int n = Nq - r0 < L.C ? Nq - r0 : L.C;
+    rc = index_common(layout, reinterpret_cast<const char*>(q_idx) + (size_t)r0 * qrow, w + (size_t)r0 * H_i,
+                      kidx_pool, idx_dtype, H_i, D_i, nullptr, q_pos + r0, seq, n, scratch, ld,
+                      base + L.off_index, L.off_topk - L.off_index, stream, status);
+    if (rc) return rc;
+    rc = topk_common(scratch, ld, n_eligible + r0, n, K, idx + (size_t)r0 * K, base + L.off_topk,
+                     L.off_attn - L.off_topk, stream, status);
+    if (rc) return rc;
+  }
+  return attn_common(layout, q, k_pool, k_row_stride, v_pool, v_row_stride, Hq, Dqk, Dv, nullptr,
+                     q_pos, Nq, idx, K, sm_scale, out, lse, base + L.off_attn,
+                     L.off_scores - L.off_attn, stream, false, status, seq);
+}
+
 }  // extern "C"

@@ -132,3 +132,37 @@ def test_noalloc_scratch_size_matches_the_header(dsa):
     want = int(m.group(1)) << int(m.group(2))
     assert int(dsa.lib().dsa_topk_noalloc_scratch_bytes()) == want
     assert dsa.TOPK_NOALLOC_SCRATCH_BYTES == want
+
+
+def test_prefill_step_chunked_workspace_holds_one_chunk_of_scores(dsa):
+    """dsa_prefill_step_chunked keeps one chunk of scores in its workspace
+    instead of the [Nq][ld] score matrix: for a 16384-token prompt the
+    automatic chunk is 768 queries (48 MB), against the 1 GiB matrix the staged
+    step's caller provides."""
+    T, K = 16384, 2048
+    staged = dsa.prefill_step_workspace_size(T, 64, 128, T, 64, 576, 512, K)
+    auto = dsa.prefill_step_chunked_workspace_size(T, 64, 128, T, 64, 576, 512, K, 0)
+    assert auto - staged <= (48 << 20) + (1 << 20)        # plus one chunk of scores
+    assert auto - staged >= 768 * T * 4                     # 768 queries of 16384 scores
+    assert dsa.prefill_step_chunked_workspace_size(T, 64, 128, T, 64, 576, 512, K, 16) < auto
+
+
+def test_prefill_step_chunked_rejects_bad_arguments(dsa):
+    lib = dsa.lib()
+    lay = _layout(dsa)
+    ws = ctypes.create_string_buffer(1 << 12)
+    base = [ctypes.byref(lay), 0, FAKE, FAKE, 8, FAKE, FAKE, 576, FAKE, FAKE, 576, FAKE, FAKE,
+            dsa.DSA_FP8_E4M3, FAKE, FAKE, 64, 128, FAKE, 64, 576, 512, 16, 0.1, 200, 0, FAKE, FAKE,
+            FAKE, ctypes.cast(ws, ctypes.c_void_p), len(ws), None]
+    def call(over=None):
+        a = list(base)
+        for k, v in (over or {}).items():
+            a[k] = v
+        return lib.dsa_prefill_step_chunked(*a)
+    before = dsa.launch_count()
+    assert call({1: 5}) == -1                     # seq outside the layout
+    assert call({25: -1}) == -1                   # chunk < 0
+    assert call({13: 99}) == -2                   # unknown indexer dtype
+    assert call({26: None}) == -1                 # idx NULL
+    assert call() == -3                           # workspace too small
+    assert dsa.launch_count() == before           # nothing launched

@@ -129,3 +129,54 @@ def test_prefill_step_in_two_chunks():
                                           c.sm_scale, Dv=c.Dv)
         assert_out_close(out, lse, o_ref, l_ref, f"chunk {lo}")
         assert dsa.get_status(ws) == 0
+
+
+@pytest.mark.parametrize("chunk", [0, 16, 112, 1000])
+def test_prefill_step_chunked_matches_the_oracle(chunk):
+    """dsa_prefill_step_chunked: the prefill step without the score matrix.
+    A 1300-token prompt (latent shapes, FP8 indexer, K = 256) is written,
+    scored and selected in chunks of `chunk` queries through one scratch
+    region (0: the automatic size, here one chunk; 16 and 112: many chunks and
+    a ragged last one), then attended; index sets and outputs are compared with
+    the oracle on every query, and with the staged step's."""
+    need_gpu()
+    dsa = lib()
+    T = 1300
+    c = W.make_case("prefill-chunked", seed=730, kind="prefill", T=T, K=256, **LAT_SHAPES)
+    bt2, nb2 = fresh_layout(c, 37, 2)
+    lay = dsa.PagedLayout(to_dev(bt2), to_dev(c.seq_lens), c.bs, nb2, T)
+    rows_k = logical_rows(c, c.k_pool, 0, T)
+    rows_i = logical_rows(c, c.kidx_pool, 0, T)
+    r = np.arange(T)
+    res = {}
+    for mode in ("chunked", "staged"):
+        k_pool = torch.zeros((nb2, c.bs, c.Dkv), dtype=torch.bfloat16, device="cuda")
+        kidx_pool = torch.zeros((nb2, c.bs, c.D_i), dtype=torch.uint8, device="cuda")
+        idx = torch.full((T, c.K), 7, dtype=torch.int32, device="cuda")
+        out = torch.empty((T, c.Hq, c.Dv), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((T, c.Hq), dtype=torch.float32, device="cuda")
+        args = (lay, 0, to_dev(c.q_pos), to_dev(c.n_elig), to_dev(rows_k), k_pool,
+                to_dev(rows_i), kidx_pool, to_dev(c.q_idx), to_dev(c.w), to_dev(c.q), c.K,
+                c.sm_scale)
+        if mode == "chunked":
+            ws = dsa.workspace(dsa.prefill_step_chunked_workspace_size(
+                T, c.H_i, c.D_i, T, c.Hq, c.Dqk, c.Dv, c.K, chunk))
+            dsa.prefill_step_chunked(*args, T, idx, out, lse, ws, chunk=chunk)
+        else:
+            scores = torch.empty((T, T), dtype=torch.float32, device="cuda")
+            ws = dsa.workspace(dsa.prefill_step_workspace_size(T, c.H_i, c.D_i, T, c.Hq, c.Dqk,
+                                                               c.Dv, c.K))
+            dsa.prefill_step(*args, scores, idx, out, lse, ws)
+        torch.cuda.synchronize()
+        assert dsa.get_status(ws) == 0
+        res[mode] = (idx.cpu().numpy(), out, lse)
+    s_ref = oracle.index_score(c.block_table, c.seq_lens, c.bs, c.num_blocks, c.q_seq, c.q_pos,
+                               c.q_idx, c.w, c.kidx_pool, code(c), T)
+    idx_ref = oracle.topk(s_ref, c.n_elig, c.K)
+    np.testing.assert_array_equal(res["chunked"][0], idx_ref)
+    np.testing.assert_array_equal(res["chunked"][0], res["staged"][0])
+    o_ref, l_ref = oracle.sparse_attn(c.block_table, c.seq_lens, c.bs, c.num_blocks, c.q_seq,
+                                      c.q, c.k_pool, c.v_pool, idx_ref, c.sm_scale, Dv=c.Dv)
+    assert_out_close(res["chunked"][1], res["chunked"][2], o_ref, l_ref, f"chunk {chunk}")
+    assert torch.equal(res["chunked"][1], res["staged"][1])
+
