@@ -25,6 +25,11 @@ cites the passage it follows:
   Heterogeneous AI Accelerators", section 4: new rows are written into the
   KV cache in the block layout, at the rows the decode gather reads (plain
   numpy, one row at a time).
+* ``page_bounds`` / ``page_score_bound`` -- "Day-0 Adaptation of
+  Trillion-Parameter MoE Models on Domestic GPUs", section 3 (3) (incremental
+  decode-time selection that reuses an index structure): per page, per key
+  dimension, the largest and smallest cached key, and the bound they give on
+  every score of the page (plain numpy, fp64, page by page).
 
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/`` against
 closed forms, invariants, library special cases and brute force; none of the
@@ -214,3 +219,67 @@ def cache_write(block_table, bs, num_blocks, seq, pos, new_rows, pool):
             continue
         out[page, p % bs, :w] = new_rows[i]
     return out, bad
+
+
+_TABLES = {}
+
+
+def _decode_table(dtype_code):
+    """Value of every code of the format (bf16: 65536 codes, E4M3: 256)."""
+    if dtype_code not in _TABLES:
+        n = 65536 if dtype_code == BF16 else 256
+        lib = _load()
+        _TABLES[dtype_code] = np.array([lib.oracle_decode(int(dtype_code), c) for c in range(n)],
+                                       dtype=np.float64)
+    return _TABLES[dtype_code]
+
+
+def page_bounds(block_table, seq_lens, bs, num_blocks, kidx_pool, dtype_code):
+    """(bounds, cached): bounds [NB, 2, D] codes (the pool's dtype) holding, for
+    every page some sequence caches a position in, per dimension the code of
+    the largest key (row 0) and of the smallest key (row 1) over the page's
+    cached positions -- the first such row on ties; cached [NB] bool marks
+    those pages (the others are zero).
+
+    "Day-0 Adaptation of Trillion-Parameter MoE Models on Domestic GPUs",
+    section 3 (3): the index structure a decode step reuses, kept per page.
+    """
+    table = _decode_table(dtype_code)
+    pool = _raw(kidx_pool, dtype_code)
+    bt = np.asarray(block_table)
+    D = pool.shape[-1]
+    out = np.zeros((num_blocks, 2, D), dtype=pool.dtype)
+    cached = np.zeros(num_blocks, dtype=bool)
+    for b in range(bt.shape[0]):
+        L = int(seq_lens[b])
+        for j in range((L + bs - 1) // bs):
+            page = int(bt[b, j])
+            n = min(bs, L - j * bs)
+            codes = pool[page, :n]                 # [n, D]
+            vals = table[codes.astype(np.int64)]
+            out[page, 0] = codes[np.argmax(vals, axis=0), np.arange(D)]
+            out[page, 1] = codes[np.argmin(vals, axis=0), np.arange(D)]
+            cached[page] = True
+    return out, cached
+
+
+def page_score_bound(q_idx, w, bounds, dtype_code):
+    """UB [NB] fp64 for one query: sum_h (w_h >= 0 ? w_h relu(hi_h) : w_h relu(lo_h))
+    with hi_h = sum_d max(q_hd kmax_d, q_hd kmin_d), lo_h the same with min, so
+    that every score of a page's cached positions is at most its UB.
+
+    q_idx: encoded [H, D]; w: [H]; bounds: [NB, 2, D] codes from page_bounds.
+    """
+    table = _decode_table(dtype_code)
+    q = table[_raw(q_idx, dtype_code).astype(np.int64)]          # [H, D]
+    kx = table[np.asarray(bounds)[:, 0].astype(np.int64)]          # [NB, D]
+    kn = table[np.asarray(bounds)[:, 1].astype(np.int64)]
+    w = np.asarray(w, dtype=np.float64)
+    ub = np.zeros(kx.shape[0])
+    for h in range(q.shape[0]):
+        u = q[h][None, :] * kx
+        v = q[h][None, :] * kn
+        hi = np.maximum(u, v).sum(axis=1)
+        lo = np.minimum(u, v).sum(axis=1)
+        ub += w[h] * np.maximum(hi if w[h] >= 0 else lo, 0.0)
+    return ub

@@ -523,3 +523,76 @@ def test_mixed_batch_row_equals_decode_of_its_prefix():
         od, _ = oracle.sparse_attn(c.block_table, sl, c.bs, c.num_blocks, [b], c.q[r:r + 1],
                                    c.k_pool, c.v_pool, idx[r:r + 1], c.sm_scale, Dv=c.Dv)
         np.testing.assert_array_equal(od[0], out[r])
+
+
+def _torch_decode(codes, dtype_code):
+    """Values of stored codes through torch's own conversions (independent of
+    the oracle's decoder)."""
+    c = np.ascontiguousarray(codes)
+    if dtype_code == oracle.BF16:
+        return torch.from_numpy(c.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    return torch.from_numpy(c.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP8_E4M3])
+def test_page_bounds_brute_force(dtype):
+    """Per page and dimension, the largest and smallest key over the page's
+    cached positions (first occurrence on ties), by plain loops over a tiny
+    permuted layout with a ragged last page and one sequence of length 1."""
+    rng = np.random.default_rng(91)
+    bs, D, seq_lens = 4, 32, (5, 8, 1)
+    pages_per = [(L + bs - 1) // bs for L in seq_lens]
+    NB = sum(pages_per) + 2
+    perm = rng.permutation(NB)
+    bt = np.full((3, 2), -1, np.int32)
+    k = 0
+    for b, n in enumerate(pages_per):
+        for j in range(n):
+            bt[b, j] = perm[k]
+            k += 1
+    vals = rng.integers(-8, 9, size=(NB, bs, D))
+    vals[0, :, 0] = 0                                # ties (and +0 / -0 for bf16 below)
+    pool = W.encode_int(vals, "bf16" if dtype == oracle.BF16 else "fp8")
+    if dtype == oracle.BF16:
+        pool[0, 1, 0] = 0x8000                       # -0.0 ties +0.0
+    got, cached = oracle.page_bounds(bt, np.array(seq_lens), bs, NB, pool, dtype)
+    for b, L in enumerate(seq_lens):
+        for j in range(pages_per[b]):
+            page = bt[b, j]
+            n = min(bs, L - j * bs)
+            assert cached[page]
+            for d in range(D):
+                v = _torch_decode(pool[page, :n, d], dtype)
+                imax = max(range(n), key=lambda r: (v[r], -r))
+                imin = min(range(n), key=lambda r: (v[r], r))
+                assert got[page, 0, d] == pool[page, imax, d]
+                assert got[page, 1, d] == pool[page, imin, d]
+    assert cached.sum() == sum(pages_per)
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP8_E4M3])
+def test_page_score_bound_holds_and_is_tight_on_constant_pages(dtype):
+    """Every score of a page's cached positions is at most the page's bound
+    (checked against the oracle's own scores, weights of both signs); a page
+    whose cached keys are all equal is bounded by exactly its score."""
+    rng = np.random.default_rng(93)
+    dname = "bf16" if dtype == oracle.BF16 else "fp8"
+    c = W.make_case("bounds", seed=94, seq_lens=(300, 130), K=16, Hq=4, Dqk=64, Dv=64,
+                    latent=False, H_i=8, D_i=32, idx_dtype=dname)
+    w = rng.integers(-3, 4, size=c.w.shape).astype(np.float32)
+    kp = c.kidx_pool.copy()
+    # page 1 of sequence 0: every cached key the same row
+    kp[c.block_table[0, 1]] = kp[c.block_table[0, 1], 0]
+    scores = oracle.index_score(c.block_table, c.seq_lens, c.bs, c.num_blocks, c.q_seq, c.q_pos,
+                                c.q_idx, w, kp, dtype, int(c.seq_lens.max()))
+    bounds, cached = oracle.page_bounds(c.block_table, c.seq_lens, c.bs, c.num_blocks, kp, dtype)
+    for b in range(c.B):
+        ub = oracle.page_score_bound(c.q_idx[b], w[b], bounds, dtype)
+        L = int(c.seq_lens[b])
+        for j in range((L + c.bs - 1) // c.bs):
+            page = c.block_table[b, j]
+            s = scores[b, j * c.bs:min(L, (j + 1) * c.bs)]
+            assert s.max() <= ub[page] + 1e-9 * max(1.0, abs(ub[page]))
+            if b == 0 and j == 1:
+                assert np.all(s == s[0])
+                assert ub[page] == pytest.approx(float(s[0]), abs=1e-9)
