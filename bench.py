@@ -362,9 +362,11 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
         stage[:, k] = [a_.elapsed_time(b_) for a_, b_ in sev]
     status = pipe.status()
     cache_write = measure_cache_write(dsa, case, d, layout, dev, flush, steps)
-    step_calls = None
+    step_calls = bounded = None
     if kind == "prefill":
         step_calls = measure_prefill_steps(dsa, case, d, layout, dev, flush, steps)
+    else:
+        bounded = measure_bounded_index(dsa, case, d, layout, dev, flush, steps, pipe.idx.clone())
 
     e2e = None
     if do_e2e:
@@ -373,7 +375,8 @@ def run_gpu(name, steps, warmup, rank, world, local_rank, do_e2e=True):
     total_ms = max_over_ranks(total_ms, world, dev)
     return dict(case=case, total_ms=total_ms, stage_ms=stage.mean(axis=0).tolist(),
                 launches=int(launches), launches_per=launches_per, clocks=clocks, status=status,
-                e2e=e2e, graph=graphs["step"], cache_write=cache_write, step_calls=step_calls)
+                e2e=e2e, graph=graphs["step"], cache_write=cache_write, step_calls=step_calls,
+                bounded_index=bounded)
 
 
 def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
@@ -418,6 +421,56 @@ def measure_cache_write(dsa, case, d, layout, dev, flush, steps):
     return {"rows": n, "bytes_per_row": int(row_bytes), "us": round(us, 2),
             "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "status": dsa.get_status(ws)}
+
+
+def measure_bounded_index(dsa, case, d, layout, dev, flush, steps, ref_idx):
+    """The decode indexer with block-level bounds (dsa_index_score_bounded): the
+    bound pool built once for every cached page (timed), then the bounded
+    scoring timed like a stage, the tiles it left out, and whether dsa_topk over
+    its row selects what the step selected."""
+    import torch
+    kb = torch.zeros((case.num_blocks, 2, case.D_i), dtype=d.kidx_pool.dtype, device=dev)
+    wsb = dsa.workspace(dsa.index_bounds_update_workspace_size(), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dsa.index_bounds_update(layout, d.kidx_pool, kb, wsb)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush(0.5)
+    e0.record(stream)
+    dsa.index_bounds_update(layout, d.kidx_pool, kb, wsb)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    build_us = e0.elapsed_time(e1) * 1e3
+    ld = (int(case.seq_lens.max()) + 3) // 4 * 4
+    scores = torch.empty((case.B, ld), dtype=torch.float32, device=dev)
+    ws = dsa.workspace(dsa.index_score_bounded_workspace_size(case.B, case.H_i, case.D_i, ld,
+                                                              case.K), device=dev)
+
+    def call():
+        dsa.index_score_bounded(layout, d.q_idx, d.w, d.kidx_pool, kb, case.K, scores, ws)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush(float(i))
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev])) * 1e3
+    skipped, total = dsa.index_bounded_stats(ws)
+    idx = torch.empty((case.B, case.K), dtype=torch.int32, device=dev)
+    wt = dsa.workspace(dsa.topk_workspace_size(case.B, ld, case.K), device=dev)
+    dsa.topk(scores, d.n_elig, case.K, idx, wt)
+    torch.cuda.synchronize()
+    return {"tiles_left_out": skipped, "tiles": total, "us": round(us, 2),
+            "bounds_build_us": round(build_us, 2),
+            "idx_equal": bool(torch.equal(idx, ref_idx)),
+            "status": dsa.get_status(ws) | dsa.get_status(wsb),
+            "api": "dsa_index_score_bounded (bound pool from dsa_index_bounds_update)"}
 
 
 def measure_prefill_steps(dsa, case, d, layout, dev, flush, steps):
@@ -752,6 +805,8 @@ def headline(args, world, res, peaks):
     }
     if res.get("step_calls") is not None:
         line["step_calls"] = res["step_calls"]
+    if res.get("bounded_index") is not None:
+        line["bounded_index"] = res["bounded_index"]
     line["path_roofline"] = path_roofline(case, ms_step, peaks)
     return line
 
@@ -785,7 +840,8 @@ def secondary_line(r2, st2, world, peaks):
             "stage_ms": dict(zip(["index_score", "topk", "sparse_attn"], r2["stage_ms"])),
             "gpu_launches": r2["launches"], "gpu_launches_per_step": r2["launches_per"],
             "clocks": r2["clocks"], "device_status": r2["status"],
-            "cache_write": r2["cache_write"], "step_calls": r2.get("step_calls")}
+            "cache_write": r2["cache_write"], "step_calls": r2.get("step_calls"),
+            "bounded_index": r2.get("bounded_index")}
 
 
 def main():

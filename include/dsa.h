@@ -363,6 +363,50 @@ int dsa_prefill_step_chunked(const dsa_paged_layout* layout, int seq, const int3
                              size_t ws_bytes, dsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block-level bounds for incremental decode indexing — "Day-0 Adaptation of
+ * Trillion-Parameter MoE Models on Domestic GPUs", section 3 (3): decode-time
+ * index selection reuses the index structure of earlier steps and computes
+ * only what is needed.  The structure is a bound pool beside the indexer-key
+ * pool: for every page, per key dimension d, the largest and the smallest key
+ * over the page's cached positions, as key codes:
+ *   kbound_pool [NB][2][D_i] in the keys' dtype (row 0 maxima, row 1 minima).
+ * dsa_index_bounds_update: recompute the bounds of the pages holding the rows
+ *   (seq[i], pos[i]), i < N — call it after dsa_cache_write with the same
+ *   seq/pos (after a decode step's append: one page per sequence) — or, with
+ *   seq = pos = NULL, of every page slot below each sequence's length.  The
+ *   layout's seq_lens must include the rows written.  ws: the status word
+ *   (dsa_index_bounds_update_workspace_size() bytes); a page id outside
+ *   [0, NB) is skipped and flags DSA_STATUS_BAD_BLOCK.
+ * dsa_index_score_bounded: the decode form of dsa_index_score (query b is the
+ *   query of sequence b, every cached position eligible, B = layout->batch,
+ *   scores [B][ld]) that leaves out 128-position tiles whose scores cannot
+ *   reach the top-K of size K: the bounds give each tile an upper bound of
+ *   its scores; the ceil(K/128) + 1 tiles with the largest bounds are scored
+ *   first, and every other tile whose bound is below the K-th largest of
+ *   those scores is left out — its scores are -inf, its keys are not read.
+ *   Every other score equals dsa_index_score's, so dsa_topk over the row
+ *   selects exactly what it selects over the full row.  Pays off only where
+ *   pages differ in their keys (on keys drawn independently per position
+ *   every bound covers the row's largest score and nothing is left out).
+ *   ws: dsa_index_score_bounded_workspace_size(B, H_i, D_i, ld, K) bytes.
+ * dsa_index_bounded_stats: after the work queued on `stream` (this call
+ *   synchronises it), the tiles the last dsa_index_score_bounded call on ws
+ *   left out and the tiles it bounded.
+ */
+size_t dsa_index_bounds_update_workspace_size(void);
+int dsa_index_bounds_update(const dsa_paged_layout* layout, const int32_t* seq,
+                            const int32_t* pos, int N, const void* kidx_pool, int D_i,
+                            int idx_dtype, void* kbound_pool, void* ws, size_t ws_bytes,
+                            dsa_stream_t stream);
+size_t dsa_index_score_bounded_workspace_size(int B, int H_i, int D_i, int64_t ld, int K);
+int dsa_index_score_bounded(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                            const void* kidx_pool, int idx_dtype, int H_i, int D_i,
+                            const void* kbound_pool, int K, float* scores, int64_t ld, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream);
+int dsa_index_bounded_stats(void* ws, dsa_stream_t stream, uint64_t* tiles_skipped,
+                            uint64_t* tiles_bounded);
+
+/* ---------------------------------------------------------------------------
  * Utilities (no counterpart on the pages).
  * dsa_get_status: copy the status word of a workspace to *status (host), after
  *   the work queued on `stream` so far has finished (this call synchronises the

@@ -98,6 +98,13 @@ _sig("dsa_prefill_step_chunked_workspace_size", _sz, [_i, _i, _i, _i64, _i, _i, 
 _sig("dsa_prefill_step_chunked", _i, [_LP, _i, _vp, _vp, _i, _vp, _vp, _i64, _vp, _vp, _i64, _vp,
                                       _vp, _i, _vp, _vp, _i, _i, _vp, _i, _i, _i, _i, _f, _i64, _i,
                                       _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("dsa_index_bounds_update_workspace_size", _sz, [])
+_sig("dsa_index_bounds_update", _i, [_LP, _vp, _vp, _i, _vp, _i, _i, _vp, _vp, _sz, _vp])
+_sig("dsa_index_score_bounded_workspace_size", _sz, [_i, _i, _i, _i64, _i])
+_sig("dsa_index_score_bounded", _i, [_LP, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _vp, _i64, _vp, _sz,
+                                     _vp])
+_sig("dsa_index_bounded_stats", _i, [_vp, _vp, ctypes.POINTER(ctypes.c_uint64),
+                                     ctypes.POINTER(ctypes.c_uint64)])
 _sig("dsa_cache_write_workspace_size", _sz, [])
 _sig("dsa_cache_write", _i, [_LP, _vp, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _i, _vp, _vp, _sz, _vp])
 _sig("dsa_sparse_attn_decode_workspace_size", _sz, [_i, _i, _i, _i, _i])
@@ -118,7 +125,10 @@ SYMBOLS = ("dsa_version", "dsa_launch_count", "dsa_last_error_string", "dsa_get_
            "dsa_cache_write_workspace_size", "dsa_cache_write",
            "dsa_decode_step_workspace_size", "dsa_decode_step",
            "dsa_prefill_step_workspace_size", "dsa_prefill_step",
-           "dsa_prefill_step_chunked_workspace_size", "dsa_prefill_step_chunked")
+           "dsa_prefill_step_chunked_workspace_size", "dsa_prefill_step_chunked",
+           "dsa_index_bounds_update_workspace_size", "dsa_index_bounds_update",
+           "dsa_index_score_bounded_workspace_size", "dsa_index_score_bounded",
+           "dsa_index_bounded_stats")
 
 
 def lib() -> ctypes.CDLL:
@@ -361,6 +371,58 @@ def cache_write(layout: PagedLayout, seq, pos, ws, kv_new=None, kv_pool=None, ki
     rc = _lib.dsa_cache_write(layout.c(), pseq, ppos, N, pkv, row_elems, pkp, stride, pin, D_i, kdt,
                               pip, pws, ws.numel(), _stream(stream))
     _check(rc, "dsa_cache_write")
+
+
+def index_bounds_update_workspace_size() -> int:
+    return int(_lib.dsa_index_bounds_update_workspace_size())
+
+
+def index_bounds_update(layout: PagedLayout, kidx_pool, kbound_pool, ws, seq=None, pos=None,
+                        stream=None):
+    """Recompute the key bounds of the pages holding rows (seq[i], pos[i]), or of
+    every cached page when seq and pos are None (include/dsa.h,
+    dsa_index_bounds_update).  kbound_pool [NB, 2, D_i] in the keys' dtype."""
+    D_i = int(kidx_pool.shape[-1])
+    N = int(seq.shape[0]) if seq is not None else 0
+    ke = (kidx_pool.element_size(),)
+    a = _Args(layout).add(seq, "seq", _I32, N).add(pos, "pos", _I32, N)
+    a.add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i))
+    a.add(kbound_pool, "kbound_pool", ke, layout.num_blocks * 2 * D_i).add(ws, "ws", _WS)
+    pseq, ppos, pk, pb, pws = a.ptrs()
+    rc = _lib.dsa_index_bounds_update(layout.c(), pseq, ppos, N, pk, D_i, _elt_dtype(kidx_pool),
+                                      pb, pws, ws.numel(), _stream(stream))
+    _check(rc, "dsa_index_bounds_update")
+
+
+def index_score_bounded_workspace_size(B, H_i, D_i, ld, K) -> int:
+    return int(_lib.dsa_index_score_bounded_workspace_size(B, H_i, D_i, ld, K))
+
+
+def index_score_bounded(layout: PagedLayout, q_idx, w, kidx_pool, kbound_pool, K, scores, ws,
+                        stream=None):
+    """Decode indexer scores that leave out the tiles which cannot reach the
+    top-K (include/dsa.h, dsa_index_score_bounded); dsa_topk over the row then
+    selects exactly what it selects over dsa_index_score's row."""
+    B, H_i, D_i = q_idx.shape
+    ld = scores.shape[1]
+    ke = (kidx_pool.element_size(),)
+    a = _Args(layout).add(q_idx, "q_idx", _KEY).add(w, "w", _F32, B * H_i)
+    a.add(kidx_pool, "kidx_pool", ke, _rows(layout, D_i))
+    a.add(kbound_pool, "kbound_pool", ke, layout.num_blocks * 2 * D_i)
+    a.add(scores, "scores", _F32, B * ld).add(ws, "ws", _WS)
+    pq, pw, pk, pb, ps, pws = a.ptrs()
+    rc = _lib.dsa_index_score_bounded(layout.c(), pq, pw, pk, _elt_dtype(kidx_pool), H_i, D_i, pb,
+                                      int(K), ps, ld, pws, ws.numel(), _stream(stream))
+    _check(rc, "dsa_index_score_bounded")
+
+
+def index_bounded_stats(ws, stream=None):
+    """(tiles left out, tiles bounded) by the last dsa_index_score_bounded call on ws."""
+    sk, tot = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    rc = _lib.dsa_index_bounded_stats(ctypes.c_void_p(ws.data_ptr()), _stream(stream),
+                                      ctypes.byref(sk), ctypes.byref(tot))
+    _check(rc, "dsa_index_bounded_stats")
+    return int(sk.value), int(tot.value)
 
 
 def decode_step_workspace_size(B, H_i, D_i, ld, Hq, Dqk, Dv, K) -> int:

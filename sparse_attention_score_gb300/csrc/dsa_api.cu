@@ -176,6 +176,85 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* n_eligible, int Nq,
   return topk_common(scores, ld, n_eligible, Nq, K, idx, ws, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------- bounds --
+size_t dsa_index_bounds_update_workspace_size(void) { return kWsHeader; }
+
+int dsa_index_bounds_update(const dsa_paged_layout* layout, const int32_t* seq,
+                            const int32_t* pos, int N, const void* kidx_pool, int D_i,
+                            int idx_dtype, void* kbound_pool, void* ws, size_t ws_bytes,
+                            dsa_stream_t stream) {
+  LayoutDev lay;
+  int rc = check_layout(layout, &lay);
+  if (rc) return rc;
+  if (!kidx_pool || !kbound_pool)
+    return set_error(DSA_ERR_INVALID, "index_bounds_update: NULL pool");
+  if ((seq == nullptr) != (pos == nullptr) || N < 0)
+    return set_error(DSA_ERR_INVALID, "index_bounds_update: seq and pos both or neither, N >= 0");
+  if ((idx_dtype != DSA_BF16 && idx_dtype != DSA_FP8_E4M3) || (D_i != 32 && D_i != 64 && D_i != 128))
+    return set_error(DSA_ERR_UNSUPPORTED,
+                     "index_bounds_update: dtype BF16/FP8_E4M3, D_i 32/64/128");
+  rc = check_ws(ws, ws_bytes, kWsHeader);
+  if (rc) return rc;
+  return index_bounds_update(lay, seq, pos, seq ? N : 0, kidx_pool, D_i, idx_dtype, kbound_pool,
+                             reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_index_score_bounded_workspace_size(int B, int H_i, int D_i, int64_t ld, int K) {
+  (void)H_i;
+  (void)D_i;
+  if (B < 1 || ld < 1 || K < 1) return kWsHeader;
+  return index_bounded_ws(B, (long long)ld, K);
+}
+
+int dsa_index_score_bounded(const dsa_paged_layout* layout, const void* q_idx, const float* w,
+                            const void* kidx_pool, int idx_dtype, int H_i, int D_i,
+                            const void* kbound_pool, int K, float* scores, int64_t ld, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream) {
+  IndexParams p{};
+  int rc = check_layout(layout, &p.lay);
+  if (rc) return rc;
+  if (ld < 1 || K < 1 || K > 65536)
+    return set_error(DSA_ERR_INVALID, "index_score_bounded: need ld >= 1, 1 <= K <= 65536");
+  if (!q_idx || !w || !kidx_pool || !kbound_pool || !scores)
+    return set_error(DSA_ERR_INVALID, "index_score_bounded: NULL tensor pointer");
+  if (!index_score_supported(idx_dtype, H_i, D_i))
+    return set_error(DSA_ERR_UNSUPPORTED,
+                     "index_score_bounded: supported dtype BF16/FP8_E4M3, H_i 1..128, D_i 32/64/128");
+  if (!aligned16(q_idx) || !aligned16(kidx_pool))
+    return set_error(DSA_ERR_INVALID,
+                     "index_score_bounded: q_idx / kidx_pool must be 16-byte aligned");
+  const int B = layout->batch;
+  rc = check_ws(ws, ws_bytes, index_bounded_ws(B, (long long)ld, K));
+  if (rc) return rc;
+  p.q_idx = q_idx;
+  p.w = w;
+  p.kidx = kidx_pool;
+  p.dtype = idx_dtype;
+  p.H = H_i;
+  p.D = D_i;
+  p.seq_const = -1;
+  p.Nq = B;
+  p.scores = scores;
+  p.ld = (long long)ld;
+  p.status = reinterpret_cast<int*>(ws);
+  return index_score_bounded(p, kbound_pool, K, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_index_bounded_stats(void* ws, dsa_stream_t stream, uint64_t* tiles_skipped,
+                            uint64_t* tiles_bounded) {
+  if (!ws || !tiles_skipped || !tiles_bounded)
+    return set_error(DSA_ERR_INVALID, "index_bounded_stats: NULL pointer");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long h[2] = {0ull, 0ull};
+  cudaError_t e = cudaMemcpyAsync(h, reinterpret_cast<char*>(ws) + kBoundedCounters, sizeof(h),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
+  *tiles_skipped = h[0];
+  *tiles_bounded = h[1];
+  return DSA_OK;
+}
+
 size_t dsa_cache_write_workspace_size(void) { return kWsHeader; }
 
 int dsa_cache_write(const dsa_paged_layout* layout, const int32_t* seq, const int32_t* pos, int N,

@@ -37,7 +37,15 @@ struct IndexParams {
   float* scores;
   long long ld;
   int* status;
+  // optional per-tile mask over positions [128 t, 128 t + 128) of query r,
+  // skip[r * skip_stride + t]: 0 score the tile, kSkipInf leave it out
+  // (scores -inf, keys not read), kSkipKeep leave it out and its scores as
+  // they are
+  const uint8_t* skip;
+  long long skip_stride;
 };
+
+constexpr uint8_t kSkipInf = 1, kSkipKeep = 2;
 
 struct TopkParams {
   const float* scores;
@@ -125,6 +133,16 @@ bool index_score_supported(int dtype, int H, int D);
 size_t index_score_ws(int Nq, int H, int D, long long ld);
 
 int launch_topk(const TopkParams& p, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// index_bounds.cu: per-page bounds of the indexer keys, and the decode
+// indexer that leaves out tiles which cannot reach the top-K.  The bounded
+// call counts skipped and bounded tiles in two uint64 of its workspace header.
+constexpr size_t kBoundedCounters = 64;
+int index_bounds_update(const LayoutDev& lay, const int32_t* seq, const int32_t* pos, int N,
+                        const void* kidx, int D, int dtype, void* kbound, int* status,
+                        cudaStream_t s);
+size_t index_bounded_ws(int B, long long ld, int K);
+int index_score_bounded(IndexParams p, const void* kbound, int K, void* ws, cudaStream_t s);
 // shared-memory block top-K (topk_smem.cu)
 bool topk_smem_eligible(long long ld, int K);
 size_t topk_smem_ws(int Nq, long long ld, int K);

@@ -68,6 +68,16 @@ __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams
   grid_dependency_wait();
   launch_dependents();
   const int r = blockIdx.y;
+  // a CTA covers one 128-position tile; a tile the caller left out is -inf
+  static_assert(kGenThreads == 128, "one skip-mask tile per CTA");
+  if (a.skip) {
+    const uint8_t m = __ldg(&a.skip[(long long)r * a.skip_stride + blockIdx.x]);
+    if (m != 0) {
+      const long long p = (long long)blockIdx.x * kGenThreads + threadIdx.x;
+      if (m == kSkipInf && p < a.ld) a.scores[(long long)r * a.ld + p] = -INFINITY;
+      return;
+    }
+  }
   float* qs = sm;
   float* ws = sm + H * D;
   for (int i = threadIdx.x; i < H * D; i += blockDim.x)

@@ -89,6 +89,11 @@ struct Cursor {
   }
 };
 
+// Tile t of query r left out by the caller's skip mask.
+__device__ __forceinline__ bool tile_skipped(const IndexParams& a, int r, long long t) {
+  return a.skip && __ldg(&a.skip[(long long)r * a.skip_stride + t]) != 0;
+}
+
 __device__ __forceinline__ void fail(Smem& s, int* status) {
   s.abort = 1;
   flag_status(status, DSA_STATUS_TIMEOUT);
@@ -211,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int item = lo; item < hi; ++item) {
         const TileLoad t = nxt;
         if (item + 1 < hi) nxt = look(item + 1);
+        // skipped tiles take no stage: the MMA issuer and the epilogue skip
+        // the same items
+        if (tile_skipped(a, t.r, t.p0 / kTileRows)) continue;
         if (t.r != cur) {
           cur = t.r;
           const int slot = nb & 1;
@@ -253,8 +261,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       c.seek(s, nq, lo);
       int cur = -1, nb = 0, stage = 0, slot = 0, it = 0;
       uint32_t phase = 0;
-      for (int item = lo; item < hi; ++item, ++it) {
+      for (int item = lo; item < hi; ++item) {
         c.advance(s, item);
+        if (tile_skipped(a, c.r, item - s.prefix[c.r])) continue;
         if (c.r != cur) {
           if (nb > 0) mma_commit(&s.bempty[(nb - 1) & 1]);
           cur = c.r;
@@ -288,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           stage = 0;
           phase ^= 1;
         }
+        ++it;
       }
       // every MMA issued by this thread must finish before TMEM is freed
       mma_commit(&s.done);
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       int cur = -1, it = 0;
       Query q{};
       float w[kHeads];
-      for (int item = lo; item < hi; ++item, ++it) {
+      for (int item = lo; item < hi; ++item) {
         c.advance(s, item);
         if (c.r != cur) {
           cur = c.r;
@@ -315,6 +325,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             w[4 * j + 2] = v.z;
             w[4 * j + 3] = v.w;
           }
+        }
+        if (tile_skipped(a, cur, item - s.prefix[cur])) {
+          const long long p = (long long)(item - s.prefix[cur]) * kTileRows + warp * 32 + lane;
+          if (p < q.n &&
+              __ldg(&a.skip[(long long)cur * a.skip_stride + (item - s.prefix[cur])]) == kSkipInf)
+            a.scores[(long long)cur * a.ld + p] = -INFINITY;
+          continue;
         }
         const int acc = it & 1;
         // warp-uniform outcome: the TMEM loads below are .sync.aligned
@@ -353,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           a.scores[(long long)cur * a.ld + p] = out;
         }
+        ++it;
       }
     }
   }
