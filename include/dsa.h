@@ -389,6 +389,7 @@ int dsa_prefill_step_chunked(const dsa_paged_layout* layout, int seq, const int3
  *   pages differ in their keys (on keys drawn independently per position
  *   every bound covers the row's largest score and nothing is left out).
  *   ws: dsa_index_score_bounded_workspace_size(B, H_i, D_i, ld, K) bytes.
+ *   B <= 65535 (DSA_ERR_UNSUPPORTED otherwise, nothing launched).
  * dsa_index_bounded_stats: after the work queued on `stream` (this call
  *   synchronises it), the tiles the last dsa_index_score_bounded call on ws
  *   left out and the tiles it bounded.

@@ -224,6 +224,8 @@ int dsa_index_score_bounded(const dsa_paged_layout* layout, const void* q_idx, c
     return set_error(DSA_ERR_INVALID,
                      "index_score_bounded: q_idx / kidx_pool must be 16-byte aligned");
   const int B = layout->batch;
+  if (B > 65535)  // the candidate gather puts the batch on the grid's y dimension
+    return set_error(DSA_ERR_UNSUPPORTED, "index_score_bounded: batch > 65535");
   rc = check_ws(ws, ws_bytes, index_bounded_ws(B, (long long)ld, K));
   if (rc) return rc;
   p.q_idx = q_idx;

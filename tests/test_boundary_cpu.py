@@ -85,6 +85,28 @@ def test_index_score_rejects_bad_arguments(dsa):
     assert "max_seq_len" in dsa.lib().dsa_last_error_string().decode()
 
 
+def test_index_score_bounded_rejects_bad_arguments(dsa):
+    """Refused before any launch: NULL tensors, K out of range, unsupported
+    shapes, a batch beyond the grid's y dimension, a short workspace."""
+    lib = dsa.lib()
+    lay = _layout(dsa)
+    ok = dsa.index_score_bounded_workspace_size(2, 4, 64, 256, 16)
+
+    def call(layout=None, kb=FAKE, K=16, D=64, ws=FAKE, wsb=ok):
+        layout = layout if layout is not None else lay
+        return lib.dsa_index_score_bounded(ctypes.byref(layout), FAKE, FAKE, FAKE, 0, 4, D, kb, K,
+                                           FAKE, 256, ws, wsb, None)
+    assert call(kb=None) == -1
+    assert call(K=0) == -1
+    assert call(K=70000) == -1
+    assert call(D=48) == -2
+    big = _layout(dsa, batch=70000)
+    assert call(layout=big) == -2
+    assert "batch" in lib.dsa_last_error_string().decode()
+    assert call(wsb=10) == -3
+    assert call(ws=None) == -3
+
+
 def test_topk_rejects_bad_arguments(dsa):
     lib = dsa.lib()
     ok = dsa.topk_workspace_size(4, 100, 8)
