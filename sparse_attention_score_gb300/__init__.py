@@ -193,9 +193,18 @@ def _rows(layout: "PagedLayout", width: int) -> int:
 _F32, _I32, _BF16, _KEY, _WS = (4,), (4,), (2,), (1, 2), (1,)  # element sizes (bytes)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    """The CUDA stream handle to launch on: `stream`, else the current stream
+    of the current device (read as a raw handle when torch offers that, which
+    costs a fraction of building a torch Stream object on every call)."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _check(rc: int, where: str):
