@@ -263,6 +263,34 @@ def test_topk_long_rows_ties_across_blocks(K):
     assert dsa.get_status(ws) == 0
 
 
+@pytest.mark.parametrize("ld,K", [(100000, 20000), (200000, 65536)])
+def test_topk_row_at_a_time_path_large_k(ld, K):
+    """K too large for the blocks' winners to fit one merge (K x blocks >
+    49152, up to the largest K the call takes): the row-at-a-time radix
+    kernel.  Ties, a constant row, NaN / +-inf / -0, rows shorter than K and
+    an empty row, against the oracle."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    assert dsa.topk_workspace_size(4, ld, K) == 256      # no block scratch: that path
+    rng = np.random.default_rng(ld + K)
+    Nq = 4
+    s = rng.integers(0, 5, size=(Nq, ld)).astype(np.float32)
+    s[1] = rng.standard_normal(ld).astype(np.float32)
+    s[1, rng.choice(ld, 40, replace=False)] = np.array(
+        [np.nan] * 10 + [np.inf] * 10 + [-np.inf] * 10 + [-0.0] * 10, np.float32)
+    s[2, :] = 2.0
+    n = np.array([ld, ld - 7, K // 2, 0], np.int32)
+    st, ne = torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda()
+    idx = torch.full((Nq, K), 7, dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(dsa.topk_workspace_size(Nq, ld, K))
+    dsa.topk(st, ne, K, idx, ws)
+    # the oracle takes only numbers; NaN ranks below every value, and row 1
+    # keeps K of its ~ld finite scores, so neither NaN nor -inf is reached
+    ref = oracle.topk(np.where(np.isnan(s), np.float32(-1e30), s), n, K)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    assert dsa.get_status(ws) == 0
+
+
 def test_topk_long_rows_short_rows_and_special_values():
     """The block + merge path on rows that leave blocks empty or short: no
     eligible position, fewer than K (then no block bounds the merge), exactly
