@@ -49,6 +49,21 @@ def test_latent_shapes_pipeline(lens, K):
     _full_check(c)
 
 
+@pytest.mark.parametrize("bs,shapes,K", [
+    (1, "tiny", 64), (16, "tiny", 256), (256, "latent", 512), (1024, "latent", 2048),
+    (48, "latent", 300),
+], ids=["bs1-tiny", "bs16-tiny", "bs256-latent", "bs1024-latent", "bs48-latent"])
+def test_pipeline_page_sizes(bs, shapes, K):
+    """Pages of other sizes than 64 positions (the tensor-core indexer's
+    page), down to one position and up to the largest size the layout takes:
+    the page table is read per position in every stage, and the indexer
+    takes its CUDA-core path."""
+    sh = TINY_SHAPES if shapes == "tiny" else LAT_SHAPES
+    c = W.make_case(f"bs{bs}", seed=350 + bs, seq_lens=(bs * 3 + 5, 2 * K + 1, 70), bs=bs, K=K,
+                    **dict(sh))
+    _full_check(c)
+
+
 def test_latent_bf16_indexer_and_extra_ld():
     shapes = dict(LAT_SHAPES, idx_dtype="bf16")
     c = W.make_case("latent-bf16", seed=301, seq_lens=(1500, 333), K=512, extra_pages=3, **shapes)
