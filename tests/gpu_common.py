@@ -76,7 +76,7 @@ def oracle_attn(case, idx, rows=None):
                               case.sm_scale, Dv=case.Dv)
 
 
-class GpuRun:
+class DevicePipeline:
     """Runs the three stages of a case on the GPU through the binding."""
 
     def __init__(self, case, dsa=None, ld=None, device="cuda"):

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import GpuRun, lib, need_gpu
+from gpu_common import DevicePipeline, lib, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,7 @@ def test_wait_that_nothing_completes_gives_up_and_reports():
     # the context is still usable: a small pipeline matches the oracle
     c = W.make_case("after-timeout", seed=900, seq_lens=(300, 129), K=64, Hq=16, Dqk=128, Dv=128,
                     latent=False, H_i=4, D_i=64, idx_dtype="bf16")
-    g = GpuRun(c, dsa=dsa)
+    g = DevicePipeline(c, dsa=dsa)
     g.all()
     s_ref = oracle.index_score(c.block_table, c.seq_lens, c.bs, c.num_blocks, c.q_seq, c.q_pos,
                                c.q_idx, c.w, c.kidx_pool, oracle.BF16, c.max_len)

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import (GpuRun, assert_out_close, assert_scores_equal, fresh_layout, lib,
+from gpu_common import (DevicePipeline, assert_out_close, assert_scores_equal, fresh_layout, lib,
                         logical_rows, need_gpu, oracle_attn, oracle_scores, to_dev, to_host)
 from workloads import device as wdev
 
@@ -79,7 +79,7 @@ def test_cache_write_decode_append_then_pipeline_matches_oracle():
     pages = c.block_table[seq, last // c.bs]
     kv_rows = c.k_pool[pages, last % c.bs].copy()
     ki_rows = c.kidx_pool[pages, last % c.bs].copy()
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     # overwrite the newest rows with garbage on the device, then append them
     garbage_kv = torch.full((c.B, c.Dkv), float("nan"), dtype=torch.bfloat16, device="cuda")
     garbage_ki = torch.full((c.B, c.D_i), 0x7F, dtype=torch.uint8, device="cuda")

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_common import GpuRun, assert_out_close, assert_scores_equal, need_gpu, oracle_attn
+from gpu_common import DevicePipeline, assert_out_close, assert_scores_equal, need_gpu, oracle_attn
 from oracle_pool import OraclePool
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -22,7 +22,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 def _gpu(c):
     """The three stages on the GPU; results copied to the host."""
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     out, lse = g.all()
     res = dict(scores=g.pipe.scores.cpu().numpy(), idx=g.pipe.idx.cpu().numpy(),
                out=out.float().cpu().numpy().astype(np.float64),

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import (GpuRun, assert_out_close, assert_scores_equal, check_topk_definition,
+from gpu_common import (DevicePipeline, assert_out_close, assert_scores_equal, check_topk_definition,
                         need_gpu, oracle_attn, oracle_scores)
 
 pytestmark = pytest.mark.gpu
@@ -22,7 +22,7 @@ LAT_SHAPES = dict(Hq=64, Dqk=576, Dv=512, latent=True, H_i=64, D_i=128, idx_dtyp
 
 def _full_check(case, ld=None):
     need_gpu()
-    g = GpuRun(case, ld=ld)
+    g = DevicePipeline(case, ld=ld)
     s = g.scores().cpu().numpy()
     s_ref = oracle_scores(case, ld=s.shape[1])
     assert_scores_equal(s, s_ref, case.n_elig)
@@ -78,7 +78,7 @@ def test_prefill_small_all_rows():
 def test_prefill_sampled_rows_k2048():
     need_gpu()
     c = W.make_case("prefill-2600", seed=401, kind="prefill", T=2600, K=2048, **LAT_SHAPES)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     out, lse = g.all()
     rows = np.array([0, 1, 63, 64, 1000, 2046, 2047, 2048, 2049, 2500, 2599])
     s_ref = oracle_scores(c, rows=rows)
@@ -119,7 +119,7 @@ def test_topk_stage_alone_heavy_ties_and_edges():
 def test_attention_stage_alone_on_oracle_indices():
     need_gpu()
     c = W.make_case("attn-only", seed=500, seq_lens=(3000, 70, 2100), K=2048, **LAT_SHAPES)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     rng = np.random.default_rng(1)
     idx = np.full((c.B, c.K), -1, np.int32)
     for b in range(c.B):
@@ -142,7 +142,7 @@ def test_edge_cases_k1_zero_weights_empty_row():
     assert idx[0].tolist() == list(range(256))       # all scores tie at 0
     # an empty row (no eligible position) gives -1 indices, zero output and -inf lse
     c3 = W.make_case("empty", seed=602, seq_lens=(200,), K=16, **TINY_SHAPES)
-    g3 = GpuRun(c3)
+    g3 = DevicePipeline(c3)
     g3.scores()
     g3.topk(n_elig=torch.zeros(1, dtype=torch.int32, device="cuda"))
     assert np.all(g3.pipe.idx.cpu().numpy() == -1)
@@ -153,7 +153,7 @@ def test_edge_cases_k1_zero_weights_empty_row():
 def test_block_table_permutation_gives_identical_results():
     need_gpu()
     c = W.make_case("perm", seed=700, seq_lens=(1200, 2500), K=512, **LAT_SHAPES)
-    g1 = GpuRun(c)
+    g1 = DevicePipeline(c)
     o1, l1 = g1.all()
     perm = np.random.default_rng(9).permutation(c.num_blocks)
     c2 = W.make_case("perm", seed=700, seq_lens=(1200, 2500), K=512, **LAT_SHAPES)
@@ -165,7 +165,7 @@ def test_block_table_permutation_gives_identical_results():
     c2.kidx_pool = ki
     c2.block_table = np.where(c2.block_table >= 0, perm[np.maximum(c2.block_table, 0)],
                               -1).astype(np.int32)
-    g2 = GpuRun(c2)
+    g2 = DevicePipeline(c2)
     o2, l2 = g2.all()
     assert torch.equal(g1.pipe.idx, g2.pipe.idx)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
@@ -176,7 +176,7 @@ def test_bad_block_id_is_flagged_not_faulted():
     import sparse_attention_score_gb300 as dsa
     c = W.make_case("bad-block", seed=800, seq_lens=(640, 300), K=64, **TINY_SHAPES)
     c.block_table[0, 3] = c.num_blocks + 1000      # positions 192..255 of sequence 0
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     s = g.scores().cpu().numpy()
     assert np.all(s[0, 192:256] == -np.inf) and np.all(np.isfinite(s[0, :192]))
     assert dsa.get_status(g.pipe.ws_index) & dsa.STATUS_BAD_BLOCK
@@ -215,7 +215,7 @@ def test_fp8_indexer_adversarial_exactness():
     c.q_idx = W.encode_int(q, "fp8")
     c.kidx_pool = W.encode_int(k, "fp8")
     c.w[:] = 4.0
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     s = g.scores().cpu().numpy()
     s_ref = oracle_scores(c, ld=s.shape[1])
     assert s_ref[np.isfinite(s_ref)].max() >= 8192 * 4
@@ -244,7 +244,7 @@ def test_attention_running_max_rescale_path():
     qf[:, 1::2, :] = -1.0
     qf[:, :, 0] = 0.0
     c.q = W.encode_bf16(qf)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     idx = np.full((c.B, c.K), -1, np.int32)
     for b in range(c.B):
         n = min(c.K, int(c.seq_lens[b]))
@@ -392,7 +392,7 @@ def test_prefill_indexer_both_entry_points():
     general form (explicit q_seq) give the oracle's scores bit for bit."""
     need_gpu()
     c = W.make_case("prefill-idx", seed=990, kind="prefill", T=1300, K=256, **LAT_SHAPES)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     s_ref = oracle_scores(c)
     assert_scores_equal(g.scores().cpu().numpy(), s_ref, c.n_elig)
     assert_scores_equal(g.scores_general().cpu().numpy(), s_ref, c.n_elig)
@@ -405,7 +405,7 @@ def test_prefill_indexer_query_subset_ragged_block():
     rows = np.sort(np.random.default_rng(4).choice(3000, 37, replace=False))
     c = W.make_case("prefill-sub", seed=991, kind="prefill", T=3000, K=512, q_rows=rows,
                     **LAT_SHAPES)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     s_ref = oracle_scores(c)
     assert_scores_equal(g.scores().cpu().numpy(), s_ref, c.n_elig)
     idx = g.topk().cpu().numpy()
@@ -425,7 +425,7 @@ def test_mixed_prefill_decode_batch_one_launch_per_stage():
     of the general entry points (explicit q_seq / q_pos)."""
     need_gpu()
     c = _mixed(600, (3000, 700, 5000, 129, 64), (100, 1, 1, 129, 64), 128)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     dsa = g.dsa
     n0 = dsa.launch_count()
     d = g.d
@@ -449,7 +449,7 @@ def test_mixed_batch_rows_do_not_interfere():
     need_gpu()
     lens, nq = (2100, 900, 300), (40, 1, 300)
     c = _mixed(610, lens, nq, 256)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     g.scores_general()
     s_all = g.pipe.scores.cpu().numpy()
     idx_all = g.topk().cpu().numpy()
@@ -464,7 +464,7 @@ def test_mixed_batch_rows_do_not_interfere():
         # the same cache, only sequence b's queries
         for f in ("q_seq", "q_pos", "n_elig", "q", "q_idx", "w"):
             setattr(solo, f, getattr(c, f)[rows])
-        gs = GpuRun(solo)
+        gs = DevicePipeline(solo)
         gs.scores_general()
         s = gs.pipe.scores.cpu().numpy()
         for r in range(n):
@@ -510,7 +510,7 @@ def test_cuda_core_attention_tiles_and_odd_shapes(name, kw, K):
     selections in random order with -1 entries anywhere."""
     need_gpu()
     c = W.make_case(name, seed=1700 + K, K=K, latent=False, H_i=4, D_i=64, idx_dtype="bf16", **kw)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     rng = np.random.default_rng(K)
     idx = _random_selection(rng, c.Nq, c.K, c.seq_lens[c.q_seq])
     out, lse = g.attn(torch.from_numpy(idx).cuda())
@@ -526,7 +526,7 @@ def test_cuda_core_attention_long_ranges_per_cta():
     rows = np.sort(np.random.default_rng(3).choice(1200, size=400, replace=False))
     c = W.make_case("long-range", seed=1750, kind="prefill", T=1200, q_rows=rows, K=600,
                     **TINY_SHAPES)
-    g = GpuRun(c)
+    g = DevicePipeline(c)
     rng = np.random.default_rng(4)
     idx = _random_selection(rng, c.Nq, c.K, c.q_pos + 1)
     out, lse = g.attn(torch.from_numpy(idx).cuda())
