@@ -27,18 +27,22 @@ def _queries(rng, n, case):
     return q, q_idx, w
 
 
-@pytest.mark.parametrize("shapes", ["latent", "tiny"])
-def test_incremental_decode_steps(shapes):
+@pytest.mark.parametrize("shapes,bs", [("latent", 64), ("tiny", 64), ("latent", 32),
+                                       ("tiny", 128)])
+def test_incremental_decode_steps(shapes, bs):
     """Three decode steps on a cache whose newest rows are not written yet:
     each step appends one row per sequence and must match the oracle on the
-    cache as it stands after that step."""
+    cache as it stands after that step (pages of 64 positions, and of 32 and
+    128, where the append lands at other in-page offsets and the indexer
+    takes its CUDA-core path)."""
     need_gpu()
     dsa = lib()
     S = 3
     if shapes == "latent":
-        c = W.make_case("steps", seed=700, seq_lens=(700, 2100, 4100), K=512, **LAT_SHAPES)
+        c = W.make_case("steps", seed=700 + bs, seq_lens=(700, 2100, 4100), K=512, bs=bs,
+                        **LAT_SHAPES)
     else:
-        c = W.make_case("steps", seed=701, seq_lens=(300, 1000, 70, 4097), K=256,
+        c = W.make_case("steps", seed=701 + bs, seq_lens=(300, 1000, 70, 4097), K=256, bs=bs,
                         Hq=16, Dqk=128, Dv=128, latent=False, H_i=4, D_i=64, idx_dtype="bf16")
     final = c.seq_lens.copy()
     B = c.B
