@@ -661,6 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!group_sync(&sm.smsync, sp, &sm.abort)) { ok = false; break; }  // l_run final
       if (!warp_wait(&sm.ofull, sa & 1, &sm.abort)) { ok = false; break; }
       tc_fence_after();
+      // this warp's 32 heads' 1 / l, read once for the four dv blocks
+      float inv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) inv[i] = s.complete ? sm.l_inv[32 * half + i] : 0.0f;
 #pragma unroll 1
       for (int q = half; q < 8; q += 2) {
         const int blk = q >> 1;
@@ -672,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat16* o = out + (size_t)(32 * half) * kDv + dv;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            o[(size_t)i * kDv] = __float2bfloat16(__uint_as_float(raw[i]) * sm.l_inv[32 * half + i]);
+            o[(size_t)i * kDv] = __float2bfloat16(__uint_as_float(raw[i]) * inv[i]);
         } else {
           float* o = po + (size_t)(32 * half) * kDv + dv;
 #pragma unroll
