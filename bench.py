@@ -531,19 +531,20 @@ def measure_prefill_steps(dsa, case, d, layout, dev, flush, steps):
     return res
 
 
-def _e2e_inputs(case, dev):
-    """The step's inputs (indexer queries, weights, block table, lengths, then
-    the attention queries) as one packed pinned host buffer, its device twin,
-    views of the twin shaped as each input (the stages read those), and the
-    offset where the attention queries start."""
+def _e2e_inputs(case, dev, extra=None):
+    """The step's inputs (indexer queries, weights, block table, lengths, any
+    `extra` arrays, then the attention queries) as one packed pinned host
+    buffer, its device twin, views of the twin shaped as each input (the
+    stages read those), and the offset where the attention queries start."""
     import torch
     parts = {
         "q_idx": (case.q_idx, torch.bfloat16 if case.idx_dtype == "bf16" else torch.uint8),
         "w": (case.w, torch.float32),
         "block_table": (case.block_table, torch.int32),
         "seq_lens": (case.seq_lens, torch.int32),
-        "q": (case.q, torch.bfloat16),
     }
+    parts.update(extra or {})
+    parts["q"] = (case.q, torch.bfloat16)
     offs, total = {}, 0
     for k, (arr, _) in parts.items():
         offs[k] = total
@@ -652,12 +653,74 @@ def run_e2e(case, d, pipe, steps, dev, flush):
                     "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
                     "h2d_copies_per_step": 2 if key == "graph" else 1, "d2h_copies_per_step": 1,
                     "out_equal": bool(torch.equal(out_host, ref_out.cpu()))}
+    if case.kind == "decode":
+        res["step"] = run_e2e_decode_step(case, d, pipe, steps, dev, flush, units, ref_out)
     res["calls"]["api"] = ("index_score, topk, sparse_attn called through the binding every "
                            "step")
     res["graph"]["api"] = ("the same calls and the copies captured once in a CUDA graph, "
                            "replayed per step, Q copied on a second stream beside the indexer "
                            "and top-K")
     return res
+
+
+def run_e2e_decode_step(case, d, pipe, steps, dev, flush, units, ref_out):
+    """The decode step as the single call a decoding loop makes
+    (dsa_decode_step: append each sequence's new K/V and indexer-key rows at
+    its last position, then index, select and attend), end to end with host
+    buffers like run_e2e's calls variant.  The rows appended are the ones
+    already cached at those positions, so the cache, and so the output, stay
+    those of the other variants; the step does the cache write on top of
+    their work."""
+    import torch
+
+    import sparse_attention_score_gb300 as dsa
+    L = case.seq_lens.astype(np.int64)
+    pages = case.block_table[np.arange(case.B), (L - 1) // case.bs]
+    rows = (L - 1) % case.bs
+    idx_t = torch.bfloat16 if case.idx_dtype == "bf16" else torch.uint8
+    extra = {"k_new": (np.ascontiguousarray(case.k_pool[pages, rows]), torch.bfloat16),
+             "kidx_new": (np.ascontiguousarray(case.kidx_pool[pages, rows]), idx_t)}
+    if not case.latent:
+        extra["v_new"] = (np.ascontiguousarray(case.v_pool[pages, rows]), torch.bfloat16)
+    hbuf, dbuf, v, total, _ = _e2e_inputs(case, dev, extra)
+    layout = dsa.PagedLayout(v["block_table"], v["seq_lens"], case.bs, case.num_blocks,
+                             case.max_len)
+    out_host = torch.empty(pipe.out.shape, dtype=pipe.out.dtype).pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    ws = dsa.workspace(dsa.decode_step_workspace_size(case.B, case.H_i, case.D_i,
+                                                      pipe.scores.shape[1], case.Hq, case.Dqk,
+                                                      case.Dv, case.K), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dbuf.copy_(hbuf, non_blocking=True)
+        dsa.decode_step(layout, v["k_new"], d.k_pool, v["kidx_new"], d.kidx_pool, v["q_idx"],
+                        v["w"], v["q"], case.K, case.sm_scale, pipe.scores, pipe.idx, pipe.out,
+                        pipe.lse, ws, v_new=v.get("v_new"),
+                        v_pool=None if case.latent else d.v_pool)
+        out_host.copy_(pipe.out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush(2.0)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return {"value": units * steps / (tot / 1e3), "unit": unit_of(case),
+            "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
+            "h2d_copies_per_step": 1, "d2h_copies_per_step": 1,
+            "out_equal": bool(torch.equal(out_host, ref_out.cpu())),
+            "status": dsa.get_status(ws),
+            "api": "dsa_decode_step, one call per step (cache append + index + top-K + "
+                   "attention)"}
 
 
 def unit_of(case):
@@ -821,6 +884,7 @@ def headline(args, world, res, peaks):
         "clocks": res["clocks"],
         "e2e": res["e2e"]["calls"] if res["e2e"] else None,
         "e2e_graph": res["e2e"]["graph"] if res["e2e"] else None,
+        "e2e_step": res["e2e"].get("step") if res["e2e"] else None,
         "gpu_launches": res["launches"],
         "gpu_launches_per_step": res["launches_per"],
         "device_status": res["status"],
