@@ -334,6 +334,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           continue;
         }
         const int acc = it & 1;
+        // this lane's position and its page id, loaded before the wait for
+        // the accumulator so that the load is not on the path to the store
+        const long long p = (long long)(item - s.prefix[cur]) * kTileRows + warp * 32 + lane;
+        const int page = p < q.n ? __ldg(&a.lay.bt[(long long)q.b * a.lay.maxb + p / 64]) : 0;
         // warp-uniform outcome: the TMEM loads below are .sync.aligned
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&s.accfull[acc], (it >> 1) & 1, &s.abort));
         if (!ok) {
@@ -360,10 +364,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tc_fence_before();
         mbar_arrive(&s.accempty[acc]);
-        const long long p = (long long)(item - s.prefix[cur]) * kTileRows + warp * 32 + lane;
         if (p < q.n) {
           float out = (sc0 + sc1) + 0.0f;
-          const int page = __ldg(&a.lay.bt[(long long)q.b * a.lay.maxb + p / 64]);
           if (page < 0 || page >= a.lay.nb) {
             flag_status(a.status, DSA_STATUS_BAD_BLOCK);
             out = -INFINITY;
