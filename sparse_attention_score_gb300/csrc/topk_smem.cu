@@ -310,20 +310,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = nchunks * K;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   int real = 0;
+  // slot q of block j keeps its key, raised by one, if it holds a winner at
+  // or above the bound (keys stay below 2^32 - 1: the largest is that of +inf)
+  auto take = [&](uint32_t v, int q, int cnt) -> uint32_t {
+    const bool in = q < cnt && v >= bound;
+    real += in ? 1 : 0;
+    return in ? v + 1u : 0u;
+  };
+  const uint32_t* src = cand_key + base;
+  if ((K & 3) == 0 && (((uintptr_t)src) & 15u) == 0) {
+    // every slot in flight at once (16-byte copies; the slots past a block's
+    // count hold stale words and are cleared below), then the keys are
+    // filtered in place; four keys of one 16-byte word share their block
+    const int n4 = total >> 2;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int j = threadIdx.x; j < n4; j += kThreads) cp_async16(keys + 4 * j, s4 + j);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    uint4* k4 = reinterpret_cast<uint4*>(keys);
 #pragma unroll 4
-  for (int i = threadIdx.x; i < total; i += kThreads) {
-    const int j = i / K, q = i - j * K;
-    uint32_t k = 0u;
-    if (q < s_cnt[j]) {
-      const uint32_t v = __ldg(&cand_key[base + i]);
-      if (v >= bound) {
-        k = v + 1u;  // keys stay below 2^32 - 1: the largest is that of +inf
-        ++real;
-      }
+    for (int j = threadIdx.x; j < n4; j += kThreads) {
+      const int i = 4 * j;
+      const int b = i / K, q = i - b * K;
+      const int cnt = s_cnt[b];
+      uint4 v = k4[j];
+      v.x = take(v.x, q, cnt);
+      v.y = take(v.y, q + 1, cnt);
+      v.z = take(v.z, q + 2, cnt);
+      v.w = take(v.w, q + 3, cnt);
+      k4[j] = v;
+      kmin = min(min(kmin, min(v.x, v.y)), min(v.z, v.w));
+      kmax = max(max(kmax, max(v.x, v.y)), max(v.z, v.w));
     }
-    keys[i] = k;
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
+  } else {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const int j = i / K, q = i - j * K;
+      const uint32_t k = take(q < s_cnt[j] ? __ldg(&cand_key[base + i]) : 0u, q, s_cnt[j]);
+      keys[i] = k;
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
   }
   // number of winners >= bound (a block-wide sum through the scan buffer)
   real = __reduce_add_sync(0xffffffffu, real);
@@ -343,10 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     need = keep_n;
     select_threshold(keys, total, kmin, kmax, T, need, sh);
   }
+  // the kept slots' indices, in output order, over the keys (emit reads every
+  // key before its first write); then their positions, all loads in flight
+  int32_t* sel = reinterpret_cast<int32_t*>(keys);
+  emit(keys, total, T, need, false, sel, (uint32_t*)nullptr, [](int i) { return i; }, sh);
+  __syncthreads();
   int32_t* out = a.idx + (long long)r * K;
-  emit(keys, total, T, need, false, out, (uint32_t*)nullptr,
-       [&](int i) { return __ldg(&cand_pos[base + i]); }, sh);
-  for (int j = keep_n + threadIdx.x; j < K; j += kThreads) out[j] = -1;
+#pragma unroll 4
+  for (int j = threadIdx.x; j < K; j += kThreads)
+    out[j] = j < keep_n ? __ldg(&cand_pos[base + sel[j]]) : -1;
 }
 
 // Grid: x = row (up to 2^31 - 1 rows), y = block of the row.
