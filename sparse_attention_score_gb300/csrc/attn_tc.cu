@@ -28,8 +28,12 @@
 // final bf16 store.
 // The tiles of all queries are laid end to end and split evenly over one CTA
 // per SM.  A query whose tiles span several CTAs leaves one unnormalised
-// partial (O, m, l) per CTA in the workspace and a second small kernel merges
-// them:  M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
+// partial (O, m, l) per CTA in the workspace and these are merged:
+// M = max m_s,  l = sum l_s 2^(m_s - M),  O = sum O_s 2^(m_s - M) / l.
+// When every query is split evenly over two or four CTAs (a decode batch: 16
+// tiles per query over four CTAs of four), those CTAs form one thread-block
+// cluster: after a cluster barrier each CTA merges its share of the query's
+// dv from the partials in L2.  Otherwise a second small kernel merges them.
 //
 // Warp roles (448 threads):
 //   warps 0-3 and 10-13 softmax, and at the end of each query segment O out
@@ -47,6 +51,9 @@
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
+#include <map>
+#include <mutex>
+
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
 #include "sm100.cuh"
@@ -74,6 +81,7 @@ constexpr int kMaxCtas = 160;
 constexpr uint32_t kIdescQK = instr_desc(128, kHq, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = instr_desc(128, kHq, 1, 1, 1, 1);
 constexpr int kPSlot = kChunks - 1;  // chunk 8 (QK only): its slot holds P^T from softmax to PV
+constexpr int kMergeBatch = 4;  // partial slots read per round trip by a merge
 
 struct __align__(1024) Smem {
   // the tile's rows, chunks 0-7 resident from QK to PV; once QK is done,
@@ -262,9 +270,84 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Cluster barrier over every thread of every CTA of the cluster (release /
+// acquire at cluster scope: the partials written before it are visible after
+// it).  Each thread of the kernel passes it exactly once, at the end, so it
+// completes once every thread has come out of its bounded waits.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Merge of the cluster's query, this CTA's share of its dv, from the CS
+// partial slots 2 c (c = the cluster's CTAs, in order), with the arithmetic
+// and order of k_attn_tc_merge (one round of CS <= kMergeBatch slots), so the
+// output is the same bit for bit.  Thread st: head st / 4; its (m, l) pairs
+// are read once and each of its two rounds has all 16 float4 loads in flight.
+// The share's float4 k * 4 + st % 4 of the head belong to the thread, so four
+// neighbouring threads read 64 contiguous bytes.
+template <int CS>
+__device__ __forceinline__ void merge_cluster_share(const AttnParams& a, const Geo& g,
+                                                    const float* part_o, const float* part_ml,
+                                                    int st) {
+  static_assert(CS >= 2 && CS <= kMergeBatch, "one merge round");
+  constexpr int kN4 = kDv / CS / 4;   // float4 of the share per head
+  constexpr int kPer = kN4 / 4;       // of them per thread
+  constexpr int kRound = 16 / CS;     // per thread per round: 16 loads in flight
+  const int rank = (int)(blockIdx.x % (unsigned)CS);
+  const int c0 = (int)blockIdx.x - rank;
+  const int r = (int)g.query_of(g.lo_of(c0));
+  const int h = st >> 2, part = st & 3;
+  const int dv0 = rank * (kDv / CS);
+  float2 ml[CS];
+#pragma unroll
+  for (int j = 0; j < CS; ++j)
+    ml[j] = __ldcg(reinterpret_cast<const float2*>(part_ml + ((size_t)2 * (c0 + j) * kHq + h) * 2));
+  float M = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < CS; ++j)
+    if (ml[j].y > 0.0f) M = fmaxf(M, ml[j].x);
+  float w[CS], L = 0.0f;
+#pragma unroll
+  for (int j = 0; j < CS; ++j) {
+    w[j] = (M > -INFINITY && ml[j].y > 0.0f) ? exp2f(ml[j].x - M) : 0.0f;
+    if (M > -INFINITY && ml[j].y > 0.0f) L = fmaf(ml[j].y, w[j], L);
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  __nv_bfloat16* o = a.out + ((size_t)r * kHq + h) * kDv + dv0;
+#pragma unroll
+  for (int k0 = 0; k0 < kPer; k0 += kRound) {
+    float4 v[CS][kRound];
+#pragma unroll
+    for (int j = 0; j < CS; ++j)
+#pragma unroll
+      for (int k = 0; k < kRound; ++k)
+        v[j][k] = __ldcg(reinterpret_cast<const float4*>(
+                             part_o + ((size_t)2 * (c0 + j) * kHq + h) * kDv + dv0) +
+                         (k0 + k) * 4 + part);
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < CS; ++j) {
+        if (M > -INFINITY && ml[j].y > 0.0f) {
+          acc.x = fmaf(w[j], v[j][k].x, acc.x); acc.y = fmaf(w[j], v[j][k].y, acc.y);
+          acc.z = fmaf(w[j], v[j][k].z, acc.z); acc.w = fmaf(w[j], v[j][k].w, acc.w);
+        }
+      }
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(o + 4 * ((k0 + k) * 4 + part)) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
+    }
+  }
+  if (a.lse && rank == 0 && part == 0)
+    a.lse[(size_t)r * kHq + h] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap map_q, AttnParams a, float* part_o,
-              float* part_ml) {
+              float* part_ml, int ccs) {
   extern __shared__ uint8_t smraw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -708,6 +791,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) fail(sm, a.status);
   }
 
+  if (ccs > 1) {
+    // every query split over this cluster's CTAs: all partials written, then
+    // each CTA merges its share (the softmax warps' 256 threads)
+    cluster_sync_all();
+    if (warp < 4 || warp >= 10) {
+      const int st = (warp < 4 ? warp : warp - 6) * 32 + lane;
+      if (ccs == 2)
+        merge_cluster_share<2>(a, g, part_o, part_ml, st);
+      else
+        merge_cluster_share<4>(a, g, part_o, part_ml, st);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -729,7 +824,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // a running maximum.  Four slots per batch keep the kernel at 80 registers,
 // three blocks per SM.
 constexpr int kMergeHeads = 4;
-constexpr int kMergeBatch = 4;
 
 __global__ void __launch_bounds__(256) k_attn_tc_merge(AttnParams a, Geo g, const float* part_o,
                                                        const float* part_ml, int by_query) {
@@ -820,6 +914,38 @@ size_t attn_tc_ws(int) {
   return kWsHeader + sizeof(float) * 2 * kMaxCtas * kHq * (kDv + 2);
 }
 
+// Largest number of clusters of `cs` attention CTAs resident at once on the
+// current device (0 if the query fails; only answers are recorded, one per
+// (device, cs)).
+static int max_active_clusters(int cs, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex m;
+  static std::map<std::pair<int, int>, int> known;
+  std::lock_guard<std::mutex> lock(m);
+  const auto key = std::make_pair(dev, cs);
+  auto it = known.find(key);
+  if (it != known.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)k_attn_tc, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the error state: this launch takes the plain path
+    return 0;
+  }
+  known[key] = n;
+  return n;
+}
+
 int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   CUtensorMap mq;
   int rc = make_tmap_2d(&mq, p.q, false, kDqk, (uint64_t)p.Nq * kHq, kDqk * 2, 64, kHq);
@@ -842,12 +968,39 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   grid = (g.total + per - 1) / per;
   g.G = (int)grid;
   g.lo = g.hi = 0;
-  cudaError_t e =
-      launch_pdl(k_attn_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mq, p, part_o, part_ml);
+  // every query on exactly cs whole CTAs (2 or 4), all clusters resident at
+  // once: the merge runs inside the attention kernel
+  int ccs = 0;
+  if (grid >= 2 && grid * per == g.total && g.Tq % per == 0) {
+    const int cs = (int)(g.Tq / per);
+    if ((cs == 2 || cs == 4) && (long long)max_active_clusters(cs, smem) * cs >= grid)
+      ccs = cs;
+  }
+  cudaError_t e;
+  if (ccs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)ccs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, k_attn_tc, mq, p, part_o, part_ml, ccs);
+  } else {
+    e = launch_pdl(k_attn_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mq, p, part_o,
+                   part_ml, 0);
+  }
   count_launch();
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   rc = check_launch("sparse_attn (tensor cores)");
-  if (rc || grid < 2) return rc;
+  if (rc || grid < 2 || ccs) return rc;
   const int by_query = p.Nq <= grid - 1 ? 1 : 0;
   e = launch_pdl(k_attn_tc_merge,
                  dim3(kHq / kMergeHeads, (unsigned)(by_query ? p.Nq : grid - 1)), dim3(256), 0, s,

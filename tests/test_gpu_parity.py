@@ -222,6 +222,43 @@ def test_fp8_indexer_adversarial_exactness():
     assert_scores_equal(s, s_ref, c.n_elig)
 
 
+@pytest.mark.parametrize("Nq,K,cs", [(64, 512, 2), (32, 2048, 4), (16, 2048, 8)])
+def test_attention_cluster_merge_splits(Nq, K, cs):
+    """Every query split evenly over cs CTAs of one thread-block cluster (on a
+    152-SM GB300: 128 CTAs, each of two or four 128-row tiles), merged inside
+    the attention kernel: outputs and lse against the oracle, with sequences
+    shorter than one CTA's share (some CTAs of a cluster hold no usable row)
+    and one of a single position.  For clusters of two and four the launch
+    count shows that no merge kernel ran; a split over eight CTAs is merged
+    by the merge kernel (clusters of eight such CTAs are not all resident at
+    once on a GB300)."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(1200 + cs)
+    lens = rng.integers(K // 2, 3 * K, size=Nq)
+    lens[:4] = (1, 100, K // 4 + 3, K)
+    c = W.make_case("cluster", seed=1300 + cs, seq_lens=tuple(int(x) for x in lens), K=K,
+                    **LAT_SHAPES)
+    idx = np.full((c.Nq, K), -1, np.int32)
+    for b in range(c.Nq):
+        L = int(c.seq_lens[b])
+        n = min(K, L)
+        idx[b, :n] = np.sort(rng.choice(L, size=n, replace=False))
+    g = DevicePipeline(c)
+    ix = torch.from_numpy(idx).cuda()
+    g.attn(ix)  # first call: one-off per-process setup
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    out, lse = g.attn(ix)
+    torch.cuda.synchronize()
+    launches = dsa.launch_count() - n0
+    out_ref, lse_ref = oracle_attn(c, idx)
+    assert_out_close(out, lse, out_ref, lse_ref, f"cluster{cs}")
+    assert g.status() == 0
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert launches == (1 if cs <= 4 else 2), launches
+
+
 def test_attention_running_max_rescale_path():
     """Scores that jump by far more than 2^8 from one 128-row tile to the next
     (for even heads only) force the O rescale in the online softmax."""
