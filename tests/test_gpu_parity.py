@@ -222,16 +222,18 @@ def test_fp8_indexer_adversarial_exactness():
     assert_scores_equal(s, s_ref, c.n_elig)
 
 
-@pytest.mark.parametrize("Nq,K,cs", [(64, 512, 2), (32, 2048, 4), (16, 2048, 8)])
+@pytest.mark.parametrize("Nq,K,cs", [(64, 512, 2), (32, 2048, 4), (16, 2048, 8), (4, 2048, 16),
+                                     (8, 2048, 16)])
 def test_attention_cluster_merge_splits(Nq, K, cs):
     """Every query split evenly over cs CTAs of one thread-block cluster (on a
-    152-SM GB300: 128 CTAs, each of two or four 128-row tiles), merged inside
-    the attention kernel: outputs and lse against the oracle, with sequences
-    shorter than one CTA's share (some CTAs of a cluster hold no usable row)
-    and one of a single position.  For clusters of two and four the launch
-    count shows that no merge kernel ran; a split over eight CTAs is merged
-    by the merge kernel (clusters of eight such CTAs are not all resident at
-    once on a GB300)."""
+    152-SM GB300: 128 CTAs of two or four 128-row tiles, or 64 and 128 CTAs
+    of one tile for 16 per query), merged inside the attention kernel:
+    outputs and lse against the oracle, with sequences shorter than one
+    CTA's share (some CTAs of a cluster hold no usable row) and one of a
+    single position.  The launch count shows whether the merge kernel ran:
+    not for clusters of 2 and 4; splits over eight or 16 CTAs are merged by
+    it (clusters of eight such CTAs are not all resident at once on a GB300,
+    and clusters of 16 measured slower than the merge kernel)."""
     need_gpu()
     import sparse_attention_score_gb300 as dsa
     rng = np.random.default_rng(1200 + cs)
