@@ -8,8 +8,12 @@
 //     z_j = sm_scale * q[r][h] . K_j,   out = sum_j softmax(z)_j V_j.
 // Softmax runs online in fp32 (log2 domain).  The K selected rows of a query
 // may be split into S ranges processed by different CTAs; each writes an
-// unnormalised partial (o, m, l) and a combine kernel merges them:
+// unnormalised partial (o, m, l) and these are merged:
 //     M = max_s m_s,  l = sum_s l_s 2^(m_s - M),  o = sum_s o_s 2^(m_s - M) / l.
+// With S <= 8 the S CTAs of a query form one thread-block cluster and merge
+// inside the kernel after a cluster barrier (CTA s: heads s, s + S, ...);
+// otherwise a combine kernel merges them.  Both merges do the same arithmetic
+// in the same order.
 //
 // This file holds the CUDA-core kernel, used for every shape the tensor-core
 // kernel (attn_tc.cu) does not cover.
@@ -60,13 +64,117 @@ __host__ __device__ inline size_t generic_smem(int Hq, int Dqk, int Dv, int T) {
          (size_t)kRowChunk * 8 + 2 * kMaxTile * 4;
 }
 
+// Merge of head h of query r from its S partials: one warp takes the (m, l)
+// of split s in lane s % 32 (S <= 64), then the weights and the denominator
+// are shared and every thread combines dims d, d + nthreads, ...  Partials
+// written by other CTAs of the kernel are read from L2.
+__device__ __forceinline__ void merge_head(const AttnParams& a, int r, int h, int S,
+                                           float* wsh, float* lsum_sh, float* mmax_sh) {
+  const int Hq = a.Hq, Dv = a.Dv;
+  if (threadIdx.x < 32) {  // lane s holds splits s and s + 32
+    const int lane = threadIdx.x;
+    float ms[2], ls[2];
+    float M = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      ms[u] = -INFINITY;
+      ls[u] = 0.0f;
+      if (s < S) {
+        const float* pml = a.part_ml + (((long long)r * S + s) * Hq + h) * 2;
+        ms[u] = __ldcg(pml);
+        ls[u] = __ldcg(pml + 1);
+        if (ls[u] > 0.0f) M = fmaxf(M, ms[u]);
+      }
+    }
+    M = warp_max(M);
+    float lsum = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      const float wgt = ls[u] > 0.0f ? exp2f(ms[u] - M) : 0.0f;
+      if (s < S) wsh[s] = wgt;
+      lsum += ls[u] * wgt;
+    }
+    lsum = warp_sum(lsum);
+    if (lane == 0) {
+      *lsum_sh = lsum;
+      *mmax_sh = M;
+    }
+  }
+  __syncthreads();
+  const float lsum = *lsum_sh;
+  const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+  for (int d = threadIdx.x; d < Dv; d += blockDim.x) {
+    float acc = 0.0f;
+    for (int s = 0; s < S; ++s)
+      acc = fmaf(wsh[s], __ldcg(&a.part_o[(((long long)r * S + s) * Hq + h) * Dv + d]), acc);
+    a.out[((long long)r * Hq + h) * Dv + d] = __float2bfloat16(acc * inv);
+  }
+  if (a.lse && threadIdx.x == 0)
+    a.lse[(long long)r * Hq + h] =
+        lsum > 0.0f ? (*mmax_sh + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  __syncthreads();  // wsh and the sums are rewritten for the next head
+}
+
+// The same merge inside the kernel for a cluster of S <= 8 CTAs: CTA `split`
+// merges heads split, split + S, ... of query r all at once.  Warp w takes
+// the weights of its heads w, w + 8, ... (as merge_head's first warp does);
+// then each thread takes one (head, dim) at a time with all S partial values
+// loaded before the fma chain, which runs in merge_head's order.
+constexpr int kClusterMax = 8;
+__device__ __forceinline__ void merge_heads_cluster(const AttnParams& a, int r, int split, int S) {
+  __shared__ float wsh[64][kClusterMax];
+  __shared__ float lsum_sh[64], mmax_sh[64];
+  const int Hq = a.Hq, Dv = a.Dv;
+  const int nh = split < Hq ? (Hq - split + S - 1) / S : 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int hh = warp; hh < nh; hh += kAttnWarps) {
+    const int h = split + hh * S;
+    float ms = -INFINITY, ls = 0.0f, M = -INFINITY;
+    if (lane < S) {
+      const float* pml = a.part_ml + (((long long)r * S + lane) * Hq + h) * 2;
+      ms = __ldcg(pml);
+      ls = __ldcg(pml + 1);
+      if (ls > 0.0f) M = ms;
+    }
+    M = warp_max(M);
+    const float wgt = ls > 0.0f ? exp2f(ms - M) : 0.0f;
+    if (lane < S) wsh[hh][lane] = wgt;
+    // merge_head's lane value (its second split, s + 32, is empty here)
+    const float lsum = warp_sum(ls * wgt);
+    if (lane == 0) {
+      lsum_sh[hh] = lsum;
+      mmax_sh[hh] = M;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nh * Dv; i += kAttnThreads) {
+    const int hh = i / Dv, d = i - hh * Dv, h = split + hh * S;
+    float v[kClusterMax];
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      v[s] = s < S ? __ldcg(&a.part_o[(((long long)r * S + s) * Hq + h) * Dv + d]) : 0.0f;
+    float acc = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      if (s < S) acc = fmaf(wsh[hh][s], v[s], acc);
+    const float lsum = lsum_sh[hh];
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+    a.out[((long long)r * Hq + h) * Dv + d] = __float2bfloat16(acc * inv);
+    if (a.lse && d == 0)
+      a.lse[(long long)r * Hq + h] =
+          lsum > 0.0f ? (mmax_sh[hh] + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
 // grid (S, Nq): CTA (split, r) takes its range of query r's selected rows in
 // tiles of T rows.  The page-table lookups of up to 256 rows run at once (one
 // thread per row); the K/V rows of tile t+1 are copied (cp.async) while tile
 // t is scored.  Warp w owns heads w, w+8, ...: in scoring lane t owns row t of
 // the tile, in the P.V product lane l owns output dims 2l, 2l+1, 2l+64, ...
 template <int HPW, int DVP>
-__global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a, int T) {
+__global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a, int T, int ccs) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int Hq = a.Hq, Dqk = a.Dqk, Dv = a.Dv;
   const int KS = Dqk + 8;  // padded K row: 16-byte reads of consecutive rows hit distinct banks
@@ -257,58 +365,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a, int
       }
     }
   }
+  if (ccs > 1) {
+    // this cluster is query r's S CTAs: every partial is written once all
+    // pass the barrier; CTA `split` then merges heads split, split + S, ...
+    cluster_sync_all();
+    merge_heads_cluster(a, r, split, S);
+  }
 }
 
 // grid (Hq, Nq): merge the S partials of one (query, head).
 __global__ void __launch_bounds__(128) k_attn_combine(AttnParams a) {
   grid_dependency_wait();
   launch_dependents();
-  const int h = blockIdx.x, r = blockIdx.y, S = a.S, Hq = a.Hq, Dv = a.Dv;
   __shared__ float wsh[kMaxSplits];
   __shared__ float lsum_sh, mmax_sh;
-  if (threadIdx.x < 32) {  // S <= 64: lane s holds splits s and s + 32
-    const int lane = threadIdx.x;
-    float ms[2], ls[2];
-    float M = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int s = lane + 32 * u;
-      ms[u] = -INFINITY;
-      ls[u] = 0.0f;
-      if (s < S) {
-        const float* pml = a.part_ml + (((long long)r * S + s) * Hq + h) * 2;
-        ms[u] = pml[0];
-        ls[u] = pml[1];
-        if (ls[u] > 0.0f) M = fmaxf(M, ms[u]);
-      }
-    }
-    M = warp_max(M);
-    float lsum = 0.0f;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int s = lane + 32 * u;
-      const float wgt = ls[u] > 0.0f ? exp2f(ms[u] - M) : 0.0f;
-      if (s < S) wsh[s] = wgt;
-      lsum += ls[u] * wgt;
-    }
-    lsum = warp_sum(lsum);
-    if (lane == 0) {
-      lsum_sh = lsum;
-      mmax_sh = M;
-    }
-  }
-  __syncthreads();
-  const float lsum = lsum_sh;
-  const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-  for (int d = threadIdx.x; d < Dv; d += blockDim.x) {
-    float acc = 0.0f;
-    for (int s = 0; s < S; ++s)
-      acc = fmaf(wsh[s], a.part_o[(((long long)r * S + s) * Hq + h) * Dv + d], acc);
-    a.out[((long long)r * Hq + h) * Dv + d] = __float2bfloat16(acc * inv);
-  }
-  if (a.lse && threadIdx.x == 0)
-    a.lse[(long long)r * Hq + h] =
-        lsum > 0.0f ? (mmax_sh + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  merge_head(a, blockIdx.y, blockIdx.x, a.S, wsh, &lsum_sh, &mmax_sh);
 }
 
 // Splits of a query's K rows: enough CTAs for two per SM, each at least one
@@ -323,26 +394,34 @@ int choose_splits(int Nq, int K) {
   return s;
 }
 
+// *merged: the splits were merged inside the kernel (clusters of S <= 8 CTAs,
+// every query's cluster resident at once), so no combine launch is needed.
 template <int HPW, int DVP>
-int launch_generic(const AttnParams& p, cudaStream_t s) {
+int launch_generic(const AttnParams& p, cudaStream_t s, bool* merged) {
   auto kern = k_attn_generic<HPW, DVP>;
   int T = kMaxTile;  // largest tile whose double buffer fits
   while (T > 1 && generic_smem(p.Hq, p.Dqk, p.Dv, T) > (size_t)kSmemLimit) T >>= 1;
   const size_t smem = generic_smem(p.Hq, p.Dqk, p.Dv, T);
   const int arc = ensure_dynamic_smem((const void*)kern, (int)smem, "sparse_attn");
   if (arc) return arc;
-  kern<<<dim3(p.S, p.Nq), kAttnThreads, smem, s>>>(p, T);
+  *merged = p.S >= 2 && p.S <= kClusterMax &&
+            max_active_clusters((const void*)kern, kAttnThreads, smem, p.S) >= p.Nq;
+  const cudaError_t e =
+      *merged ? launch_pdl_cluster(kern, dim3(p.S, p.Nq), dim3(kAttnThreads), smem, p.S, s, p, T,
+                                   p.S)
+              : launch_pdl(kern, dim3(p.S, p.Nq), dim3(kAttnThreads), smem, s, p, T, 0);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("sparse_attn");
 }
 
 template <int HPW>
-int launch_dv(const AttnParams& p, cudaStream_t s) {
+int launch_dv(const AttnParams& p, cudaStream_t s, bool* merged) {
   const int dvp = (p.Dv + 63) / 64;  // bf16 pairs per lane
-  if (dvp <= 1) return launch_generic<HPW, 1>(p, s);
-  if (dvp <= 2) return launch_generic<HPW, 2>(p, s);
-  if (dvp <= 4) return launch_generic<HPW, 4>(p, s);
-  return launch_generic<HPW, 8>(p, s);
+  if (dvp <= 1) return launch_generic<HPW, 1>(p, s, merged);
+  if (dvp <= 2) return launch_generic<HPW, 2>(p, s, merged);
+  if (dvp <= 4) return launch_generic<HPW, 4>(p, s, merged);
+  return launch_generic<HPW, 8>(p, s, merged);
 }
 
 }  // namespace
@@ -370,14 +449,16 @@ int launch_attn(AttnParams p, bool /*decode*/, void* ws, size_t ws_bytes, cudaSt
     p.part_ml = p.part_o + (size_t)p.Nq * p.S * p.Hq * p.Dv;
   }
   const int hpw = (p.Hq + kAttnWarps - 1) / kAttnWarps;
+  bool merged = false;
   int rc;
-  if (hpw <= 1) rc = launch_dv<1>(p, s);
-  else if (hpw <= 2) rc = launch_dv<2>(p, s);
-  else if (hpw <= 4) rc = launch_dv<4>(p, s);
-  else rc = launch_dv<8>(p, s);
-  if (rc != DSA_OK || p.S == 1) return rc;
-  k_attn_combine<<<dim3(p.Hq, p.Nq), 128, 0, s>>>(p);
+  if (hpw <= 1) rc = launch_dv<1>(p, s, &merged);
+  else if (hpw <= 2) rc = launch_dv<2>(p, s, &merged);
+  else if (hpw <= 4) rc = launch_dv<4>(p, s, &merged);
+  else rc = launch_dv<8>(p, s, &merged);
+  if (rc != DSA_OK || p.S == 1 || merged) return rc;
+  const cudaError_t e = launch_pdl(k_attn_combine, dim3(p.Hq, p.Nq), dim3(128), 0, s, p);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("sparse_attn combine");
 }
 

@@ -51,9 +51,6 @@
 // Selected rows that are padding, past the sequence, non-causal or behind a
 // bad block id are copied as zeros and masked to -inf.
 // Every wait is bounded (DSA_STATUS_TIMEOUT, then the CTA winds down).
-#include <map>
-#include <mutex>
-
 #include "device_common.cuh"
 #include "dsa_internal.cuh"
 #include "sm100.cuh"
@@ -268,15 +265,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Cluster barrier over every thread of every CTA of the cluster (release /
-// acquire at cluster scope: the partials written before it are visible after
-// it).  Each thread of the kernel passes it exactly once, at the end, so it
-// completes once every thread has come out of its bounded waits.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Merge of the cluster's query, this CTA's share of its dv, from the CS
@@ -914,38 +902,6 @@ size_t attn_tc_ws(int) {
   return kWsHeader + sizeof(float) * 2 * kMaxCtas * kHq * (kDv + 2);
 }
 
-// Largest number of clusters of `cs` attention CTAs resident at once on the
-// current device (0 if the query fails; only answers are recorded, one per
-// (device, cs)).
-static int max_active_clusters(int cs, size_t smem) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static std::mutex m;
-  static std::map<std::pair<int, int>, int> known;
-  std::lock_guard<std::mutex> lock(m);
-  const auto key = std::make_pair(dev, cs);
-  auto it = known.find(key);
-  if (it != known.end()) return it->second;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)cs);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)k_attn_tc, &cfg) != cudaSuccess) {
-    cudaGetLastError();  // clear the error state: this launch takes the plain path
-    return 0;
-  }
-  known[key] = n;
-  return n;
-}
-
 int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   CUtensorMap mq;
   int rc = make_tmap_2d(&mq, p.q, false, kDqk, (uint64_t)p.Nq * kHq, kDqk * 2, 64, kHq);
@@ -973,26 +929,14 @@ int launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t s) {
   int ccs = 0;
   if (grid >= 2 && grid * per == g.total && g.Tq % per == 0) {
     const int cs = (int)(g.Tq / per);
-    if ((cs == 2 || cs == 4) && (long long)max_active_clusters(cs, smem) * cs >= grid)
+    if ((cs == 2 || cs == 4) &&
+        (long long)max_active_clusters((const void*)k_attn_tc, kThreads, smem, cs) * cs >= grid)
       ccs = cs;
   }
   cudaError_t e;
   if (ccs) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)ccs;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, k_attn_tc, mq, p, part_o, part_ml, ccs);
+    e = launch_pdl_cluster(k_attn_tc, dim3((unsigned)grid), dim3(kThreads), smem, ccs, s, mq, p,
+                           part_o, part_ml, ccs);
   } else {
     e = launch_pdl(k_attn_tc, dim3((unsigned)grid), dim3(kThreads), smem, s, mq, p, part_o,
                    part_ml, 0);

@@ -21,6 +21,15 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Barrier over every thread of every CTA of the thread-block cluster, with
+// release / acquire at cluster scope: global writes before it are visible to
+// the cluster's threads after it.  A kernel that takes it passes it exactly
+// once in every thread, after all its own waits, so it cannot block past them.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(int* status, int bit) {
   if (status) atomicOr(status, bit);
 }

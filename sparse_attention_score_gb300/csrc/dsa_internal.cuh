@@ -97,6 +97,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same launch with its CTAs grouped in clusters of `cs` along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               int cs, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cs;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // selftest.cu
 int bounded_wait_selftest(int expire, unsigned long long limit_ns, int* status, cudaStream_t s);
 
@@ -120,6 +141,10 @@ int sm_count();  // of the current device
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device (once per kernel and device, thread-safe); DSA_ERR_CUDA on failure.
 int ensure_dynamic_smem(const void* kernel, int bytes, const char* what);
+// Largest number of clusters of `cs` CTAs (1-D, `threads` each, `smem` bytes of
+// dynamic shared memory) of `kernel` resident at once on the current device;
+// 0 if the query fails.  Answers are recorded per (kernel, device, shape).
+int max_active_clusters(const void* kernel, int threads, size_t smem, int cs);
 
 // launchers: return DSA_OK / DSA_ERR_*
 int launch_index_score(const IndexParams& p, cudaStream_t s);

@@ -261,6 +261,40 @@ def test_attention_cluster_merge_splits(Nq, K, cs):
         assert launches == (1 if cs <= 4 else 2), launches
 
 
+@pytest.mark.parametrize("Nq,K,launches", [(1, 64, 1), (1, 256, 1), (3, 512, 2), (1, 2048, 2)],
+                         ids=["S2-cluster", "S8-cluster", "S16-combine", "S64-combine"])
+def test_cuda_core_attention_split_merges(Nq, K, launches):
+    """The CUDA-core attention (16 heads x 128, separate K and V pools) splits
+    each query's rows over S = min(304 / Nq, K / 32, 64) CTAs: with S <= 8
+    they form a thread-block cluster and merge inside the kernel (one
+    launch), otherwise the combine kernel merges them (two).  Outputs and lse
+    against the oracle, with a sequence shorter than one split's share."""
+    need_gpu()
+    import sparse_attention_score_gb300 as dsa
+    rng = np.random.default_rng(1400 + K + Nq)
+    lens = [int(x) for x in rng.integers(K, 3 * K, size=Nq)]
+    lens[0] = max(1, K // 9)
+    c = W.make_case("split", seed=1500 + K, seq_lens=tuple(lens), K=K, **TINY_SHAPES)
+    idx = np.full((c.Nq, K), -1, np.int32)
+    for b in range(c.Nq):
+        L = int(c.seq_lens[b])
+        n = min(K, L)
+        idx[b, :n] = np.sort(rng.choice(L, size=n, replace=False))
+    g = DevicePipeline(c)
+    ix = torch.from_numpy(idx).cuda()
+    g.attn(ix)
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    out, lse = g.attn(ix)
+    torch.cuda.synchronize()
+    got = dsa.launch_count() - n0
+    out_ref, lse_ref = oracle_attn(c, idx)
+    assert_out_close(out, lse, out_ref, lse_ref, f"split K={K}")
+    assert g.status() == 0
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert got == launches, got
+
+
 def test_attention_running_max_rescale_path():
     """Scores that jump by far more than 2^8 from one 128-row tile to the next
     (for even heads only) force the O rescale in the online softmax."""
