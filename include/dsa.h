@@ -272,7 +272,9 @@ int dsa_sparse_attn_prefill(const dsa_paged_layout* layout, const void* q, const
  *  kidx_pool   [num_blocks][block_size][D_i] of kidx_dtype
  *  ws          workspace of dsa_cache_write_workspace_size() bytes
  * Pointers 16-byte aligned.  Rows of the same physical row written twice in
- * one call: one of them wins (unspecified which).
+ * one call (a caller error the call does not detect): each 16-byte piece of
+ * that row holds the piece of one of them, which one unspecified, so the row
+ * may mix them.
  * Errors: DSA_ERR_INVALID for null pointers, N < 0, bad sizes, strides or
  * alignment.  Device: a sequence outside [0, batch), a position outside the
  * block table or a block id outside [0, num_blocks) skips that row and sets

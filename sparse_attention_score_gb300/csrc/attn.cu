@@ -121,12 +121,16 @@ __device__ __forceinline__ void merge_head(const AttnParams& a, int r, int h, in
 // merges heads split, split + S, ... of query r all at once.  Warp w takes
 // the weights of its heads w, w + 8, ... (as merge_head's first warp does);
 // then each thread takes one (head, dim) at a time with all S partial values
-// loaded before the fma chain, which runs in merge_head's order.
+// loaded before the fma chain, which runs in merge_head's order.  scratch:
+// 10 Hq floats of the CTA's dynamic shared memory, free once the tiles are
+// done (the kernel's smallest dynamic allocation, 3.3 KB, holds 40 B x 64).
 constexpr int kClusterMax = 8;
-__device__ __forceinline__ void merge_heads_cluster(const AttnParams& a, int r, int split, int S) {
-  __shared__ float wsh[64][kClusterMax];
-  __shared__ float lsum_sh[64], mmax_sh[64];
+__device__ __forceinline__ void merge_heads_cluster(const AttnParams& a, int r, int split, int S,
+                                                    float* scratch) {
   const int Hq = a.Hq, Dv = a.Dv;
+  float* wsh = scratch;                 // [Hq][kClusterMax]
+  float* lsum_sh = wsh + Hq * kClusterMax;
+  float* mmax_sh = lsum_sh + Hq;
   const int nh = split < Hq ? (Hq - split + S - 1) / S : 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int hh = warp; hh < nh; hh += kAttnWarps) {
@@ -140,7 +144,7 @@ __device__ __forceinline__ void merge_heads_cluster(const AttnParams& a, int r, 
     }
     M = warp_max(M);
     const float wgt = ls > 0.0f ? exp2f(ms - M) : 0.0f;
-    if (lane < S) wsh[hh][lane] = wgt;
+    if (lane < S) wsh[hh * kClusterMax + lane] = wgt;
     // merge_head's lane value (its second split, s + 32, is empty here)
     const float lsum = warp_sum(ls * wgt);
     if (lane == 0) {
@@ -158,7 +162,7 @@ __device__ __forceinline__ void merge_heads_cluster(const AttnParams& a, int r, 
     float acc = 0.0f;
 #pragma unroll
     for (int s = 0; s < kClusterMax; ++s)
-      if (s < S) acc = fmaf(wsh[hh][s], v[s], acc);
+      if (s < S) acc = fmaf(wsh[hh * kClusterMax + s], v[s], acc);
     const float lsum = lsum_sh[hh];
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
     a.out[((long long)r * Hq + h) * Dv + d] = __float2bfloat16(acc * inv);
@@ -367,9 +371,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_generic(AttnParams a, int
   }
   if (ccs > 1) {
     // this cluster is query r's S CTAs: every partial is written once all
-    // pass the barrier; CTA `split` then merges heads split, split + S, ...
+    // pass the barrier (which also ends this CTA's use of its tile buffers);
+    // CTA `split` then merges heads split, split + S, ...
     cluster_sync_all();
-    merge_heads_cluster(a, r, split, S);
+    merge_heads_cluster(a, r, split, S, reinterpret_cast<float*>(smraw));
   }
 }
 

@@ -60,7 +60,10 @@ __device__ __forceinline__ void load_row(const void* base, long long off, float 
 }
 
 // One thread per position; grid (ceil(ld/128), Nq).  The query's indexer
-// heads and weights sit in shared memory and are read as broadcasts.
+// heads and weights sit in shared memory and are read as broadcasts.  Each
+// thread's sequence length, causal bound and block-table entry are loaded
+// before the heads (none depends on another), so the chain to its key row is
+// one load deep.
 template <int D, int DT>
 __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams a) {
   extern __shared__ float sm[];
@@ -78,6 +81,17 @@ __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams
       return;
     }
   }
+  const long long p = (long long)blockIdx.x * kGenThreads + threadIdx.x;
+  const int b = a.seq_const >= 0 ? a.seq_const : (a.q_seq ? __ldg(&a.q_seq[r]) : r);
+  const bool b_ok = b >= 0 && b < a.lay.batch;
+  long long L = 0, qp = 0;
+  int page = -1;
+  if (b_ok) {
+    L = __ldg(&a.lay.seq_lens[b]);
+    if (a.q_pos) qp = __ldg(&a.q_pos[r]);
+    const long long slot = p / a.lay.bs;
+    if (p < a.ld && slot < a.lay.maxb) page = __ldg(&a.lay.bt[(long long)b * a.lay.maxb + slot]);
+  }
   float* qs = sm;
   float* ws = sm + H * D;
   for (int i = threadIdx.x; i < H * D; i += blockDim.x)
@@ -85,21 +99,20 @@ __global__ void __launch_bounds__(kGenThreads) k_index_score_generic(IndexParams
   for (int i = threadIdx.x; i < H; i += blockDim.x) ws[i] = __ldg(&a.w[(long long)r * H + i]);
   __syncthreads();
 
-  const long long p = (long long)blockIdx.x * kGenThreads + threadIdx.x;
   if (p >= a.ld) return;
-  const int b = a.seq_const >= 0 ? a.seq_const : (a.q_seq ? __ldg(&a.q_seq[r]) : r);
   float out = -INFINITY;
-  if (b >= 0 && b < a.lay.batch) {
-    long long L = __ldg(&a.lay.seq_lens[b]);
+  if (b_ok) {
     const long long cap = (long long)a.lay.maxb * a.lay.bs;
     if (L > cap || L > a.ld) {
       if (p == 0) flag_status(a.status, DSA_STATUS_BAD_LENGTH);
       L = L < cap ? L : cap;
     }
-    long long last = a.q_pos ? (long long)__ldg(&a.q_pos[r]) : L - 1;
+    long long last = a.q_pos ? qp : L - 1;
     if (last > L - 1) last = L - 1;
     if (p <= last) {
-      const long long row = phys_row(a.lay.bt, a.lay.maxb, a.lay.bs, a.lay.nb, b, p);
+      // phys_row with the entry loaded above
+      const long long row =
+          page >= 0 && page < a.lay.nb ? (long long)page * a.lay.bs + p % a.lay.bs : -1;
       if (row < 0) {
         flag_status(a.status, DSA_STATUS_BAD_BLOCK);
       } else {
@@ -128,8 +141,9 @@ int launch_generic(const IndexParams& p, cudaStream_t s) {
   const int arc = ensure_dynamic_smem((const void*)kern, 96 * 1024, "index_score");
   if (arc) return arc;
   dim3 grid((unsigned)((p.ld + kGenThreads - 1) / kGenThreads), (unsigned)p.Nq);
-  kern<<<grid, kGenThreads, smem, s>>>(p);
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kGenThreads), smem, s, p);
   count_launch();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return check_launch("index_score");
 }
 
